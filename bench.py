@@ -1,0 +1,348 @@
+#!/usr/bin/env python
+"""Benchmark of RoPE-on-load paged attention (position-free KV cache) on GB300.
+
+Default workload: decode over RAG contexts, 64 requests x 8192 tokens, 32/8
+heads, d 128, bf16 (the Llama-3-8B attention shape).  One step = one decode
+call over the whole batch (all steps of the hot path: query rotation, paged
+gather, key rotation, split-KV attention, log-sum-exp merge).  Prints one JSON
+line.  ``--impl reference`` times the CPU float64 oracle on a bounded sample of
+the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RoPE-on-load paged attn: decode HBM GB/s (% peak), prefill TFLOP/s (% peak)"
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="minipic", choices=["minipic", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the rope-off, e2e and CPU legs")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU oracle sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.f is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(parts)
+            except Exception:
+                pass
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def decode_kv_bytes(w) -> int:
+    """Algorithmic bytes of one decode step: every request reads its own K and V
+    (logical, gathered) rows once: sum_r seq_len_r * Hkv * d * 2 * elem."""
+    el = 2 if w.dtype == "bf16" else 4
+    return int(w.decode.seq_lens.astype("int64").sum()) * w.Hkv * w.d * 2 * el
+
+
+def unique_kv_bytes(w) -> int:
+    el = 2 if w.dtype == "bf16" else 4
+    return int(w.unique_blocks) * w.Hkv * w.block_size * w.d * 2 * el
+
+
+def workload_desc(w) -> dict:
+    d = w.decode
+    return {"workload": f"{w.name}: {w.notes}", "batch": int(d.batch), "Hq": w.Hq, "Hkv": w.Hkv,
+            "head_dim": w.d, "block_size": w.block_size, "rope_base": w.rope_base,
+            "max_seq_len": int(d.seq_lens.max()), "dtype": w.dtype}
+
+
+# ---------------------------------------------------------------------- CPU oracle legs
+
+def oracle_sample(w, budget_s: float, max_requests=None):
+    """Time the float64 oracle on whole requests until ~budget_s has elapsed."""
+    import oracle
+    n = 0
+    nbytes = 0
+    el = 2 if w.dtype == "bf16" else 4
+    t0 = time.perf_counter()
+    for r in range(w.decode.batch):
+        oracle.decode(w, requests=[r])
+        n += 1
+        nbytes += int(w.decode.seq_lens[r]) * w.Hkv * w.d * 2 * el
+        if time.perf_counter() - t0 >= budget_s or (max_requests and n >= max_requests):
+            break
+    dt = time.perf_counter() - t0
+    return nbytes, dt, n
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import workloads as W
+    w = W.rag_decode(0)
+    el = 2 if w.dtype == "bf16" else 4
+    per_req = [int(w.decode.seq_lens[r]) * w.Hkv * w.d * 2 * el for r in range(w.decode.batch)]
+    import oracle
+    for i in range(args.warmup):
+        oracle.decode(w, requests=[i % w.decode.batch])
+    times = []
+    nbytes = 0
+    for i in range(args.steps):
+        r = (args.warmup + i) % w.decode.batch
+        t0 = time.perf_counter()
+        oracle.decode(w, requests=[r])
+        times.append(time.perf_counter() - t0)
+        nbytes += per_req[r]
+    total = sum(times)
+    value = nbytes / total / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": dict(workload_desc(w), sample="one request of the batch per step"),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one whole request (8192 keys x 8 kv heads) per step, numpy float64"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- GPU legs
+
+def run_minipic(args):
+    import numpy as np
+    import torch
+
+    import position_independent_kv_paged_gb300 as mp
+    import workloads as W
+    from position_independent_kv_paged_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    mp.load()
+    pk = peaks()
+
+    # the workload: each rank decodes its own batch (weak scaling, no data-path collective)
+    w = W.rag_decode(seed=rank)
+    d = w.decode
+
+    def up(a):
+        if w.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    kpool, vpool = up(w.kv.k_pool), up(w.kv.v_pool)
+    q = up(d.q)
+    bt = torch.from_numpy(d.block_tables).to(dev)
+    st = torch.from_numpy(d.block_starts).to(dev)
+    sl = torch.from_numpy(d.seq_lens).to(dev)
+    qp = torch.from_numpy(d.q_pos).to(dev)
+    rope = mp.rope_table(w.max_pos, w.d, w.rope_base, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(d.batch, w.Hq, dtype=torch.float32, device=dev)
+    ws_n = mp.decode_workspace_size(d.batch, w.Hq, w.Hkv, w.d, bt.shape[1])
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    nbytes = decode_kv_bytes(w)
+
+    def step():
+        mp.attn_decode(q, kpool, vpool, bt, st, sl, qp, rope, out=out, lse=lse, workspace=ws)
+
+    def step_norope():
+        mp.attn_decode_prerotated(q, kpool, vpool, bt, st, sl, qp, out=out, lse=lse, workspace=ws)
+
+    def timed(fn, steps):
+        evs = []
+        for _ in range(steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if mp.device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t_wall = time.perf_counter()
+        ms = timed(step, args.steps)
+        t_wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms_step = sum(ms) / len(ms)
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = nbytes * world / (ms_step * 1e-3) / 1e9
+    achieved = nbytes / (ms_step * 1e-3) / 1e9
+    n_split = (ws_n > 0)
+    kernels_per_step = 2 if n_split else 1
+
+    extras = {}
+    e2e = None
+    cpu = None
+    if not args.no_extras:
+        # rotation compiled out, same inputs and memory traffic
+        for _ in range(3):
+            step_norope()
+        ms_nr = timed(step_norope, args.steps)
+        ms_nr = sum(ms_nr) / len(ms_nr)
+        extras["rope_off"] = {"ms_per_step": ms_nr, "rope_overhead": ms_step / ms_nr - 1.0,
+                              "note": "same kernel with rotation compiled out (pre-rotated cache)"}
+        # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+        hq = torch.from_numpy(np.ascontiguousarray(d.q).view(np.int16)).view(torch.bfloat16).pin_memory()
+        hbt = torch.from_numpy(d.block_tables).pin_memory()
+        hst = torch.from_numpy(d.block_starts).pin_memory()
+        hsl = torch.from_numpy(d.seq_lens).pin_memory()
+        hqp = torch.from_numpy(d.q_pos).pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hst, hsl, hqp))
+        d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            bt.copy_(hbt, non_blocking=True)
+            st.copy_(hst, non_blocking=True)
+            sl.copy_(hsl, non_blocking=True)
+            qp.copy_(hqp, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        ms_e2e = timed(e2e_step, args.steps)
+        ms_e2e = sum(ms_e2e) / len(ms_e2e)
+        e2e = {"value": nbytes * world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+               "note": "pinned host q/tables -> device, decode call, out/lse -> pinned host; KV pool resident"}
+        if rank == 0 and world == 1:
+            nb, dt, nreq = oracle_sample(w, args.cpu_seconds)
+            cpu = {"value": nb / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{nreq} whole request(s) of this batch (numpy float64, single thread), {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(workload_desc(w), parallelism=f"replicas{world}" if world > 1 else "single",
+                           l2=f"flushed before every step by writing {L2_FLUSH_BYTES >> 20} MiB",
+                           logical_kv_bytes=nbytes, unique_kv_bytes=unique_kv_bytes(w)),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm"], "traffic": None,
+                         "peak_source": pk["src"], "kernel": "decode (split + merge launches of one call)"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": kernels_per_step * args.steps,
+            "clocks": clk.summary(),
+            "wall_s_timed": t_wall,
+        }
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_minipic(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

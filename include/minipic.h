@@ -1,0 +1,206 @@
+/*
+ * minipic.h -- C ABI of the position-free paged attention library (GB300, sm_103a).
+ *
+ * The library implements the attention step of MiniPIC's position-free KV cache
+ * (MiniPIC summary, gist.science/it/paper/2606.13126, section 2.1): keys are
+ * stored unrotated (k~_j) in a paged block pool, and the kernels apply rotary
+ * position embedding on the fly at each request's logical key position pi(j):
+ *
+ *     score(t, j) = (R_t q_t)^T (R_{pi(j)} k~_j) / sqrt(d)
+ *     out_t       = sum_j softmax_j(score(t, .)) v_j
+ *
+ * The rotation is applied with a cosine/sine table lookup and multiply-adds per
+ * key element (same section, "Implementazione"), so one physical block can be
+ * read by several concurrent requests at different offsets without being
+ * rewritten ("Vantaggio").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Rotary form: half rotation.  For i < d/2 and angle a = p * theta_i with
+ *    theta_i = base^(-2 i / d):
+ *        x'_i       = x_i       cos a - x_{i+d/2} sin a
+ *        x'_{i+d/2} = x_{i+d/2} cos a + x_i       sin a
+ *  - KV pool: k_pool and v_pool are device arrays [num_blocks][num_kv_heads]
+ *    [block_size][head_dim] of the call's dtype; keys are NOT rotated.
+ *  - Request r's key with request-local index j lives in physical block
+ *    block_tables[r*max_blocks_per_seq + j/block_size], slot j % block_size,
+ *    at logical position pi(j) = block_starts[r*max_blocks_per_seq + j/block_size]
+ *    + j % block_size.  Both tables are device int32 [batch][max_blocks_per_seq].
+ *  - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *  - Queries are passed unrotated with their positions; the kernels rotate them.
+ *  - The rotary table is the device array written by minipic_rope_table:
+ *    float [max_pos][head_dim], cos(p theta_i) in columns [0, d/2) and
+ *    sin(p theta_i) in columns [d/2, d).  Every position used must be < max_pos.
+ *  - scale <= 0 selects 1/sqrt(head_dim).
+ *  - Outputs: out has the layout of q and the call's dtype; lse (optional, may
+ *    be NULL) is float, natural-log log-sum-exp of the scaled scores per
+ *    (query token, query head).  A query with no key gets out = 0, lse = -inf.
+ *  - Supported: head_dim 64 or 128, block_size 16, num_q_heads a multiple of
+ *    num_kv_heads with num_q_heads / num_kv_heads <= 16, dtype f32 or bf16
+ *    (prefill and mixed: bf16 only).  All device pointers 16-byte aligned.
+ *
+ * Ownership and execution
+ * -----------------------
+ *  The caller owns every buffer.  The library allocates no device memory; entry
+ *  points that need scratch take a caller-provided workspace whose size is given
+ *  by the matching *_workspace_size query.  All calls are asynchronous on the
+ *  given stream (cudaStream_t; NULL = legacy default stream) and act on the
+ *  device current at the call.  Inputs must stay valid until the work completes.
+ *
+ * Errors
+ * ------
+ *  Every entry point returns a minipic_status; nothing aborts or throws across
+ *  the ABI and no kernel traps.  Host-side validation failures return before
+ *  any launch.  Device data (block ids, positions, lengths) is checked inside
+ *  the kernels: an out-of-range block id or position is skipped (treated as a
+ *  masked key) and a bit is set in a device error word that
+ *  minipic_device_error() reads and clears.
+ */
+#ifndef MINIPIC_H
+#define MINIPIC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* minipic_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MINIPIC_OK = 0,
+  MINIPIC_ERR_INVALID = 1,      /* an argument is null, negative, misaligned or inconsistent */
+  MINIPIC_ERR_UNSUPPORTED = 2,  /* a valid configuration this build has no kernel for */
+  MINIPIC_ERR_WORKSPACE = 3,    /* workspace is NULL or smaller than the size query returned */
+  MINIPIC_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+  MINIPIC_ERR_DEVICE_CHECK = 5  /* a kernel recorded out-of-range device data (see below) */
+} minipic_status;
+
+typedef enum { MINIPIC_F32 = 0, MINIPIC_BF16 = 1 } minipic_dtype;
+
+/* Bits of the device error word. */
+#define MINIPIC_DEVERR_BLOCK_ID   1  /* a block table entry outside [0, num_blocks) */
+#define MINIPIC_DEVERR_POSITION   2  /* a key or query position outside [0, max_pos) */
+#define MINIPIC_DEVERR_SEQ_LEN    4  /* a length above max_blocks_per_seq * block_size or negative */
+
+/* The paged KV pool (device memory, caller-owned). */
+typedef struct {
+  const void* k_pool;     /* [num_blocks][num_kv_heads][block_size][head_dim], unrotated keys */
+  const void* v_pool;     /* same layout, values */
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  int32_t block_size;     /* must be 16 */
+  int32_t head_dim;       /* 64 or 128 */
+} minipic_kv_pool;
+
+/* The rotary cos/sin table written by minipic_rope_table (device memory). */
+typedef struct {
+  const float* cos_sin;   /* [max_pos][head_dim] */
+  int32_t max_pos;
+  int32_t head_dim;       /* must equal the pool's head_dim */
+} minipic_rope;
+
+/* One decode token per request (MiniPIC section 2.1 score equation with the
+ * query at position q_pos[r] over all seq_lens[r] stored keys of request r). */
+typedef struct {
+  const void* q;                /* [batch][num_q_heads][head_dim], unrotated */
+  const int32_t* block_tables;  /* [batch][max_blocks_per_seq] physical block ids */
+  const int32_t* block_starts;  /* [batch][max_blocks_per_seq] logical start position of each block */
+  const int32_t* seq_lens;      /* [batch] number of stored keys of each request */
+  const int32_t* q_pos;         /* [batch] position of each decode token */
+  int32_t batch;
+  int32_t max_blocks_per_seq;   /* row stride of the tables; seq_lens[r] <= this * block_size */
+  void* out;                    /* [batch][num_q_heads][head_dim] */
+  float* lse;                   /* [batch][num_q_heads] or NULL */
+} minipic_decode_batch;
+
+/* Chunked prefill: request r's query chunk is rows cu_q_lens[r] .. cu_q_lens[r+1]-1
+ * of q; it attends to the request's kv_lens[r] stored keys, which include the
+ * chunk's own keys as the last q_len ones.  Query i of the chunk sees keys
+ * j <= kv_lens[r] - q_len + i (causal, bottom-right aligned by key index). */
+typedef struct {
+  const void* q;                /* [total_q][num_q_heads][head_dim], unrotated */
+  const int32_t* cu_q_lens;     /* [batch + 1], cu_q_lens[0] = 0 */
+  const int32_t* q_pos;         /* [total_q] position of each query token */
+  const int32_t* block_tables;  /* [batch][max_blocks_per_seq] */
+  const int32_t* block_starts;  /* [batch][max_blocks_per_seq] */
+  const int32_t* kv_lens;       /* [batch], kv_lens[r] >= q_len of request r */
+  int32_t batch;
+  int32_t total_q;              /* cu_q_lens[batch] */
+  int32_t max_q_len;            /* an upper bound of every chunk length (grid planning) */
+  int32_t max_blocks_per_seq;
+  void* out;                    /* [total_q][num_q_heads][head_dim] */
+  float* lse;                   /* [total_q][num_q_heads] or NULL */
+} minipic_prefill_batch;
+
+/* Human-readable name of a status code (static string). */
+const char* minipic_status_string(minipic_status status);
+
+/* Fill the rotary table (MiniPIC section 2.1, "a cosine/sine table"):
+ * cos_sin[p*head_dim + i] = cos(p theta_i), cos_sin[p*head_dim + d/2 + i] =
+ * sin(p theta_i), theta_i = rope_base^(-2 i / head_dim), for 0 <= p < max_pos.
+ * The angle p * theta_i is formed in double precision and the result rounded
+ * to float.  cos_sin: device, at least max_pos * head_dim floats, caller-owned.
+ * Errors: INVALID for null/misaligned/non-positive sizes/odd head_dim or
+ * rope_base <= 0; CUDA on launch failure. */
+minipic_status minipic_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim,
+                                  double rope_base, minipic_stream_t stream);
+
+/* Workspace bytes minipic_attn_decode needs for this shape on the current
+ * device (split-KV partial results).  0 means no workspace is needed.  The
+ * value depends only on the arguments and the device's SM count. */
+size_t minipic_attn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t max_blocks_per_seq,
+                                          int32_t block_size);
+
+/* Decode attention over the position-free paged cache (split-KV with a
+ * log-sum-exp merge of the splits).  Rotates q at q_pos and every gathered key
+ * at its pi(j) from the table.  dtype selects f32 or bf16 for q, pools and out
+ * (arithmetic is fp32; bf16 uses tensor-core products with bf16 operands).
+ * workspace: device, >= minipic_attn_decode_workspace_size(...) bytes
+ * (may be NULL when that size is 0).  Errors: INVALID, UNSUPPORTED, WORKSPACE,
+ * CUDA; device-data problems are reported by minipic_device_error. */
+minipic_status minipic_attn_decode(minipic_dtype dtype, int32_t num_q_heads,
+                                   const minipic_kv_pool* kv, const minipic_rope* rope,
+                                   const minipic_decode_batch* batch, float scale,
+                                   void* workspace, size_t workspace_bytes,
+                                   minipic_stream_t stream);
+
+/* The same decode kernel with the rotation compiled out: keys in the pool and
+ * q are taken as already rotated (standard paged attention over a pre-rotated
+ * cache).  It exists to measure what on-the-fly rotation costs against
+ * identical memory traffic; rope may be NULL.  Same errors as above. */
+minipic_status minipic_attn_decode_prerotated(minipic_dtype dtype, int32_t num_q_heads,
+                                              const minipic_kv_pool* kv,
+                                              const minipic_decode_batch* batch, float scale,
+                                              void* workspace, size_t workspace_bytes,
+                                              minipic_stream_t stream);
+
+/* Workspace bytes minipic_attn_prefill needs (0 in this build). */
+size_t minipic_attn_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t max_q_len,
+                                           int32_t max_blocks_per_seq, int32_t block_size);
+
+/* Chunked prefill over cached span blocks plus the chunk's own keys (the
+ * uncached-span prefill of MiniPIC section 4 and the final-prompt prefill that
+ * reads cached spans).  Keys are rotated at pi(j) into shared memory and the
+ * products run on the tcgen05 tensor cores with TMEM accumulators.  bf16 only
+ * (f32 returns UNSUPPORTED).  Errors as for decode. */
+minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads,
+                                    const minipic_kv_pool* kv, const minipic_rope* rope,
+                                    const minipic_prefill_batch* batch, float scale,
+                                    void* workspace, size_t workspace_bytes,
+                                    minipic_stream_t stream);
+
+/* Read the device error word (MINIPIC_DEVERR_* bits, 0 if none) of the current
+ * device after the work queued on `stream` has finished (this call
+ * synchronizes the stream), and reset it to 0 when `clear` is nonzero.
+ * Returns DEVICE_CHECK if any bit was set, OK otherwise, CUDA on failure. */
+minipic_status minipic_device_error(int32_t* flags_out, int32_t clear, minipic_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MINIPIC_H */

@@ -114,10 +114,13 @@ def decode(w, requests: Optional[Iterable[int]] = None, scale: float = 0.0):
     for r in (range(B) if requests is None else requests):
         n = int(dec.seq_lens[r])
         qr = rope_rotate(widen(dec.q[r], w.dtype), [int(dec.q_pos[r])] * w.Hq, w.rope_base)
+        phys, slot, pos = key_index_map(dec.block_tables[r], dec.block_starts[r], n, w.block_size)
+        # all kv heads of the request at once: [Hkv, n, d], rotated at pos
+        k = np.swapaxes(widen(w.kv.k_pool[phys, :, slot], w.dtype), 0, 1)
+        v = np.swapaxes(widen(w.kv.v_pool[phys, :, slot], w.dtype), 0, 1)
+        kr = rope_rotate(k, pos, w.rope_base)
         for g in range(w.Hkv):
-            k, v, pos = _gathered(w, dec.block_tables[r], dec.block_starts[r], n, g)
-            kr = rope_rotate(k, pos, w.rope_base)
-            o, l = attend(qr[g * G:(g + 1) * G], kr, v, sc)
+            o, l = attend(qr[g * G:(g + 1) * G], kr[g], v[g], sc)
             out[r, g * G:(g + 1) * G] = o
             lse[r, g * G:(g + 1) * G] = l
     return out, lse

@@ -1,0 +1,296 @@
+"""Position-free paged attention for GB300 (sm_103a): Python binding.
+
+This module only marshals arguments to the C ABI of ``libminipic.so`` (declared
+in ``include/minipic.h``); every step of the attention runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current CUDA stream.
+There is no CPU fallback: if the library is missing or fails to load, every
+call raises ``MiniPICError``.
+
+Conventions (see the header for the full contract): the paged pools are
+``[num_blocks, num_kv_heads, block_size, head_dim]`` and hold UNROTATED keys;
+request r's key j lives in block ``block_tables[r, j // 16]`` at logical
+position ``block_starts[r, j // 16] + j % 16``; queries are passed unrotated
+with their positions; the kernels rotate both with the cos/sin table built by
+``rope_table`` (half-rotation RoPE, theta_i = base^(-2i/d)).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+__all__ = [
+    "MiniPICError",
+    "library_path",
+    "load",
+    "rope_table",
+    "decode_workspace_size",
+    "attn_decode",
+    "attn_decode_prerotated",
+    "prefill_workspace_size",
+    "attn_prefill",
+    "device_error",
+    "STATUS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libminipic.so")
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+          3: "workspace missing or too small", 4: "CUDA error", 5: "device data out of range"}
+F32, BF16 = 0, 1
+
+
+class MiniPICError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, 'unknown')} (status {self.status})")
+
+
+class _KV(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class _Rope(ctypes.Structure):
+    _fields_ = [("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class _Decode(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("block_tables", ctypes.c_void_p),
+                ("block_starts", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("q_pos", ctypes.c_void_p), ("batch", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("out", ctypes.c_void_p),
+                ("lse", ctypes.c_void_p)]
+
+
+class _Prefill(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("cu_q_lens", ctypes.c_void_p), ("q_pos", ctypes.c_void_p),
+                ("block_tables", ctypes.c_void_p), ("block_starts", ctypes.c_void_p),
+                ("kv_lens", ctypes.c_void_p), ("batch", ctypes.c_int32), ("total_q", ctypes.c_int32),
+                ("max_q_len", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libminipic.so (once) and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise MiniPICError(4, f"libminipic.so not found at {p}; build it with "
+                                  "position_independent_kv_paged_gb300._build.build()")
+        L = ctypes.CDLL(p)
+        c_i32, c_sz, c_vp, c_f, c_d = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float, ctypes.c_double
+        L.minipic_status_string.restype = ctypes.c_char_p
+        L.minipic_status_string.argtypes = [ctypes.c_int]
+        L.minipic_rope_table.restype = ctypes.c_int
+        L.minipic_rope_table.argtypes = [c_vp, c_i32, c_i32, c_d, c_vp]
+        L.minipic_attn_decode_workspace_size.restype = c_sz
+        L.minipic_attn_decode_workspace_size.argtypes = [c_i32] * 6
+        L.minipic_attn_decode.restype = ctypes.c_int
+        L.minipic_attn_decode.argtypes = [ctypes.c_int, c_i32, ctypes.POINTER(_KV), ctypes.POINTER(_Rope),
+                                          ctypes.POINTER(_Decode), c_f, c_vp, c_sz, c_vp]
+        L.minipic_attn_decode_prerotated.restype = ctypes.c_int
+        L.minipic_attn_decode_prerotated.argtypes = [ctypes.c_int, c_i32, ctypes.POINTER(_KV),
+                                                     ctypes.POINTER(_Decode), c_f, c_vp, c_sz, c_vp]
+        L.minipic_attn_prefill_workspace_size.restype = c_sz
+        L.minipic_attn_prefill_workspace_size.argtypes = [c_i32] * 7
+        L.minipic_attn_prefill.restype = ctypes.c_int
+        L.minipic_attn_prefill.argtypes = [ctypes.c_int, c_i32, ctypes.POINTER(_KV), ctypes.POINTER(_Rope),
+                                           ctypes.POINTER(_Prefill), c_f, c_vp, c_sz, c_vp]
+        L.minipic_device_error.restype = ctypes.c_int
+        L.minipic_device_error.argtypes = [ctypes.POINTER(c_i32), c_i32, c_vp]
+        _lib = L
+        return L
+
+
+# ---------------------------------------------------------------- helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _need(t, name, dtype=None, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MiniPICError(status, where)
+
+
+def _kv(k_pool, v_pool) -> _KV:
+    _need(k_pool, "k_pool", ndim=4)
+    _need(v_pool, "v_pool", dtype=k_pool.dtype, ndim=4)
+    if tuple(k_pool.shape) != tuple(v_pool.shape):
+        raise ValueError("k_pool and v_pool shapes differ")
+    nb, hkv, bs, d = k_pool.shape
+    return _KV(k_pool.data_ptr(), v_pool.data_ptr(), nb, hkv, bs, d)
+
+
+# ---------------------------------------------------------------- API
+
+def rope_table(max_pos: int, head_dim: int, base: float, device=None, stream=None, out=None):
+    """Build the fp32 cos/sin table [max_pos, head_dim] on the GPU."""
+    torch = _torch()
+    L = load()
+    if out is None:
+        out = torch.empty((max_pos, head_dim), dtype=torch.float32,
+                          device=device if device is not None else "cuda")
+    _need(out, "out", dtype=torch.float32, ndim=2)
+    _check(L.minipic_rope_table(out.data_ptr(), int(max_pos), int(head_dim), float(base), _stream(stream)),
+           "minipic_rope_table")
+    return out
+
+
+def decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                          max_blocks_per_seq: int, block_size: int = 16) -> int:
+    return int(load().minipic_attn_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                         max_blocks_per_seq, block_size))
+
+
+def _decode(q, k_pool, v_pool, block_tables, block_starts, seq_lens, q_pos, rope, scale, out, lse,
+            workspace, stream, prerotated):
+    torch = _torch()
+    L = load()
+    _need(q, "q", ndim=3)
+    kv = _kv(k_pool, v_pool)
+    if k_pool.dtype != q.dtype:
+        raise TypeError("q and the pools must share a dtype")
+    B, Hq, d = q.shape
+    for name, t in (("block_tables", block_tables), ("block_starts", block_starts)):
+        _need(t, name, dtype=torch.int32, ndim=2)
+    _need(seq_lens, "seq_lens", dtype=torch.int32, ndim=1)
+    _need(q_pos, "q_pos", dtype=torch.int32, ndim=1)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dtype=q.dtype)
+    if lse is not None:
+        _need(lse, "lse", dtype=torch.float32)
+    mb = block_tables.shape[1]
+    if workspace is None:
+        n = decode_workspace_size(B, Hq, kv.num_kv_heads, d, mb, kv.block_size)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    db = _Decode(q.data_ptr(), block_tables.data_ptr(), block_starts.data_ptr(), seq_lens.data_ptr(),
+                 q_pos.data_ptr(), B, mb, out.data_ptr(), _ptr(lse))
+    ws_ptr, ws_n = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if prerotated:
+        st = L.minipic_attn_decode_prerotated(_dtype_code(q), Hq, ctypes.byref(kv), ctypes.byref(db),
+                                              float(scale), ws_ptr, ws_n, _stream(stream))
+        _check(st, "minipic_attn_decode_prerotated")
+    else:
+        _need(rope, "rope", dtype=torch.float32, ndim=2)
+        rp = _Rope(rope.data_ptr(), rope.shape[0], rope.shape[1])
+        st = L.minipic_attn_decode(_dtype_code(q), Hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(db),
+                                   float(scale), ws_ptr, ws_n, _stream(stream))
+        _check(st, "minipic_attn_decode")
+    return out, lse
+
+
+def attn_decode(q, k_pool, v_pool, block_tables, block_starts, seq_lens, q_pos, rope, scale: float = 0.0,
+                out=None, lse=None, workspace=None, stream=None):
+    """One decode token per request over the position-free paged cache.
+
+    Returns (out, lse); out has q's shape/dtype, lse is the optional float
+    [B, Hq] log-sum-exp buffer passed in (None if not given)."""
+    return _decode(q, k_pool, v_pool, block_tables, block_starts, seq_lens, q_pos, rope, scale, out, lse,
+                   workspace, stream, False)
+
+
+def attn_decode_prerotated(q, k_pool, v_pool, block_tables, block_starts, seq_lens, q_pos,
+                           scale: float = 0.0, out=None, lse=None, workspace=None, stream=None):
+    """Same kernel with rotation compiled out (keys and q already rotated)."""
+    return _decode(q, k_pool, v_pool, block_tables, block_starts, seq_lens, q_pos, None, scale, out, lse,
+                   workspace, stream, True)
+
+
+def prefill_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_q_len, max_blocks_per_seq,
+                           block_size=16) -> int:
+    return int(load().minipic_attn_prefill_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                          max_q_len, max_blocks_per_seq, block_size))
+
+
+def attn_prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv_lens, rope,
+                 max_q_len: int, scale: float = 0.0, out=None, lse=None, workspace=None, stream=None):
+    """Chunked prefill (bf16) over cached span blocks plus the chunk's own keys."""
+    torch = _torch()
+    L = load()
+    _need(q, "q", ndim=3)
+    kv = _kv(k_pool, v_pool)
+    total_q, Hq, d = q.shape
+    for name, t in (("block_tables", block_tables), ("block_starts", block_starts)):
+        _need(t, name, dtype=torch.int32, ndim=2)
+    for name, t in (("cu_q_lens", cu_q_lens), ("q_pos", q_pos), ("kv_lens", kv_lens)):
+        _need(t, name, dtype=torch.int32, ndim=1)
+    _need(rope, "rope", dtype=torch.float32, ndim=2)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _need(lse, "lse", dtype=torch.float32)
+    B = kv_lens.shape[0]
+    mb = block_tables.shape[1]
+    if workspace is None:
+        n = prefill_workspace_size(B, Hq, kv.num_kv_heads, d, max_q_len, mb, kv.block_size)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    pb = _Prefill(q.data_ptr(), cu_q_lens.data_ptr(), q_pos.data_ptr(), block_tables.data_ptr(),
+                  block_starts.data_ptr(), kv_lens.data_ptr(), B, total_q, int(max_q_len), mb,
+                  out.data_ptr(), _ptr(lse))
+    rp = _Rope(rope.data_ptr(), rope.shape[0], rope.shape[1])
+    st = L.minipic_attn_prefill(_dtype_code(q), Hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(pb),
+                                float(scale), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "minipic_attn_prefill")
+    return out, lse
+
+
+def device_error(clear: bool = True, stream=None) -> int:
+    """Device error word (MINIPIC_DEVERR_* bits) after the stream's work."""
+    flags = ctypes.c_int32(0)
+    st = load().minipic_device_error(ctypes.byref(flags), 1 if clear else 0, _stream(stream))
+    if st not in (0, 5):
+        raise MiniPICError(st, "minipic_device_error")
+    return int(flags.value)

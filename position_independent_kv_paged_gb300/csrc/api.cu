@@ -1,0 +1,272 @@
+// C-ABI layer: argument validation, split planning, workspace sizing and
+// launches.  No allocation, no state except the per-device error word.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <mutex>
+
+#include "../../include/minipic.h"
+#include "internal.h"
+
+namespace minipic {
+
+// Device error word (MINIPIC_DEVERR_* bits); one per device that loads the library.
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {nullptr};
+int g_num_sms[kMaxDevices] = {0};
+std::mutex g_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device lookups done once: the device address of the error word and the SM count.
+cudaError_t device_info(int** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_num_sms[dev] = n;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (sms) *sms = g_num_sms[dev];
+  return cudaSuccess;
+}
+
+int current_sms() {
+  int sms = 0;
+  if (device_info(nullptr, &sms) != cudaSuccess || sms <= 0) sms = 152;
+  return sms;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DecodeWs {
+  size_t o_bytes, ml_bytes, total;
+};
+
+DecodeWs decode_ws(int batch, int Hq, int D, int n_split) {
+  DecodeWs w{0, 0, 0};
+  if (n_split <= 1) return w;
+  w.o_bytes = align_up((size_t)batch * Hq * n_split * D * sizeof(float), 256);
+  w.ml_bytes = align_up((size_t)batch * Hq * n_split * 2 * sizeof(float), 256);
+  w.total = w.o_bytes + w.ml_bytes;
+  return w;
+}
+
+minipic_status check_pool(const minipic_kv_pool* kv, int32_t num_q_heads, bool need_ptrs) {
+  if (!kv) return MINIPIC_ERR_INVALID;
+  if (kv->num_blocks < 0 || kv->num_kv_heads <= 0 || num_q_heads <= 0) return MINIPIC_ERR_INVALID;
+  if (num_q_heads % kv->num_kv_heads != 0) return MINIPIC_ERR_INVALID;
+  if (kv->head_dim <= 0 || (kv->head_dim & 1)) return MINIPIC_ERR_INVALID;
+  if (kv->block_size <= 0) return MINIPIC_ERR_INVALID;
+  if (need_ptrs && kv->num_blocks > 0) {
+    if (!kv->k_pool || !kv->v_pool) return MINIPIC_ERR_INVALID;
+    if (!aligned16(kv->k_pool) || !aligned16(kv->v_pool)) return MINIPIC_ERR_INVALID;
+  }
+  if (kv->head_dim != 64 && kv->head_dim != 128) return MINIPIC_ERR_UNSUPPORTED;
+  if (kv->block_size != 16) return MINIPIC_ERR_UNSUPPORTED;
+  if (num_q_heads / kv->num_kv_heads > 16) return MINIPIC_ERR_UNSUPPORTED;
+  return MINIPIC_OK;
+}
+
+minipic_status check_rope(const minipic_rope* rope, int head_dim) {
+  if (!rope || !rope->cos_sin || !aligned16(rope->cos_sin)) return MINIPIC_ERR_INVALID;
+  if (rope->max_pos <= 0 || rope->head_dim != head_dim) return MINIPIC_ERR_INVALID;
+  return MINIPIC_OK;
+}
+
+minipic_status decode_common(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                             const minipic_rope* rope, const minipic_decode_batch* b, float scale,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                             bool rotate) {
+  if (dtype != MINIPIC_F32 && dtype != MINIPIC_BF16) return MINIPIC_ERR_INVALID;
+  if (!b) return MINIPIC_ERR_INVALID;
+  minipic_status st = check_pool(kv, num_q_heads, b->batch > 0);
+  if (st != MINIPIC_OK) return st;
+  if (b->batch < 0 || b->max_blocks_per_seq < 0) return MINIPIC_ERR_INVALID;
+  if (rotate) {
+    st = check_rope(rope, kv->head_dim);
+    if (st != MINIPIC_OK) return st;
+  }
+  if (b->batch == 0) return MINIPIC_OK;
+  if (b->max_blocks_per_seq == 0) return MINIPIC_ERR_INVALID;
+  if (!b->q || !b->block_tables || !b->block_starts || !b->seq_lens || !b->q_pos || !b->out)
+    return MINIPIC_ERR_INVALID;
+  if (!aligned16(b->q) || !aligned16(b->out) || !aligned16(b->block_tables) ||
+      !aligned16(b->block_starts))
+    return MINIPIC_ERR_INVALID;
+  if (!isfinite(scale)) return MINIPIC_ERR_INVALID;
+
+  int* err = nullptr;
+  int sms = 0;
+  if (device_info(&err, &sms) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  const bool bf16 = dtype == MINIPIC_BF16;
+  const int G = num_q_heads / kv->num_kv_heads;
+  DecodePlan plan = plan_decode(b->batch, kv->num_kv_heads, G, kv->head_dim, b->max_blocks_per_seq,
+                                kv->block_size, bf16, sms);
+  DecodeWs ws = decode_ws(b->batch, num_q_heads, kv->head_dim, plan.n_split);
+  if (ws.total > 0) {
+    if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return MINIPIC_ERR_WORKSPACE;
+  }
+
+  DecodeArgs a{};
+  a.q = b->q;
+  a.k_pool = kv->k_pool;
+  a.v_pool = kv->v_pool;
+  a.block_tables = b->block_tables;
+  a.block_starts = b->block_starts;
+  a.seq_lens = b->seq_lens;
+  a.q_pos = b->q_pos;
+  a.cos_sin = rotate ? rope->cos_sin : nullptr;
+  a.max_pos = rotate ? rope->max_pos : 0;
+  a.out = b->out;
+  a.lse = b->lse;
+  a.part_o = ws.total ? static_cast<float*>(workspace) : nullptr;
+  a.part_ml = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_bytes) : nullptr;
+  a.batch = b->batch;
+  a.Hq = num_q_heads;
+  a.Hkv = kv->num_kv_heads;
+  a.G = G;
+  a.D = kv->head_dim;
+  a.BS = kv->block_size;
+  a.num_blocks = kv->num_blocks;
+  a.max_blocks = b->max_blocks_per_seq;
+  a.split_blocks = plan.split_blocks;
+  a.n_split = plan.n_split;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)kv->head_dim);
+  a.err = err;
+  cudaError_t e = launch_decode(a, bf16, rotate, plan, stream);
+  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs, bool bf16, int num_sms) {
+  (void)G;
+  (void)D;
+  (void)bs;
+  (void)bf16;
+  DecodePlan p{max_blocks, 1, false};
+  const long long pairs = (long long)batch * Hkv;
+  const long long target = (long long)num_sms * 4;
+  const int min_split_blocks = 8;
+  if (pairs >= target || max_blocks <= min_split_blocks) return p;
+  long long n = (target + pairs - 1) / pairs;
+  const long long cap = (max_blocks + min_split_blocks - 1) / min_split_blocks;
+  if (n > cap) n = cap;
+  if (n < 1) n = 1;
+  p.split_blocks = (int)((max_blocks + n - 1) / n);
+  p.n_split = (max_blocks + p.split_blocks - 1) / p.split_blocks;
+  return p;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, bool bf16, bool rotate, const DecodePlan& plan,
+                          cudaStream_t s) {
+  (void)plan;
+  cudaError_t e = launch_decode_simt(a, bf16, rotate, s);
+  if (e != cudaSuccess) return e;
+  return launch_decode_merge(a, bf16, s);
+}
+
+}  // namespace minipic
+
+using namespace minipic;
+
+extern "C" {
+
+const char* minipic_status_string(minipic_status status) {
+  switch (status) {
+    case MINIPIC_OK: return "ok";
+    case MINIPIC_ERR_INVALID: return "invalid argument";
+    case MINIPIC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MINIPIC_ERR_WORKSPACE: return "workspace missing or too small";
+    case MINIPIC_ERR_CUDA: return "CUDA error";
+    case MINIPIC_ERR_DEVICE_CHECK: return "device data out of range";
+  }
+  return "unknown status";
+}
+
+minipic_status minipic_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double rope_base,
+                                  minipic_stream_t stream) {
+  if (!cos_sin || !aligned16(cos_sin) || max_pos <= 0 || head_dim <= 0 || (head_dim & 1))
+    return MINIPIC_ERR_INVALID;
+  if (!(rope_base > 0.0) || !isfinite(rope_base)) return MINIPIC_ERR_INVALID;
+  cudaError_t e = launch_rope_table(cos_sin, max_pos, head_dim, rope_base, (cudaStream_t)stream);
+  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
+size_t minipic_attn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t max_blocks_per_seq,
+                                          int32_t block_size) {
+  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+      block_size <= 0 || num_q_heads % num_kv_heads)
+    return 0;
+  const int G = num_q_heads / num_kv_heads;
+  DecodePlan p = plan_decode(batch, num_kv_heads, G, head_dim, max_blocks_per_seq, block_size, true,
+                             current_sms());
+  DecodePlan p32 = plan_decode(batch, num_kv_heads, G, head_dim, max_blocks_per_seq, block_size, false,
+                               current_sms());
+  const size_t a = decode_ws(batch, num_q_heads, head_dim, p.n_split).total;
+  const size_t b = decode_ws(batch, num_q_heads, head_dim, p32.n_split).total;
+  return a > b ? a : b;
+}
+
+minipic_status minipic_attn_decode(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                                   const minipic_rope* rope, const minipic_decode_batch* batch, float scale,
+                                   void* workspace, size_t workspace_bytes, minipic_stream_t stream) {
+  return decode_common(dtype, num_q_heads, kv, rope, batch, scale, workspace, workspace_bytes,
+                       (cudaStream_t)stream, true);
+}
+
+minipic_status minipic_attn_decode_prerotated(minipic_dtype dtype, int32_t num_q_heads,
+                                              const minipic_kv_pool* kv, const minipic_decode_batch* batch,
+                                              float scale, void* workspace, size_t workspace_bytes,
+                                              minipic_stream_t stream) {
+  return decode_common(dtype, num_q_heads, kv, nullptr, batch, scale, workspace, workspace_bytes,
+                       (cudaStream_t)stream, false);
+}
+
+size_t minipic_attn_prefill_workspace_size(int32_t, int32_t, int32_t, int32_t, int32_t, int32_t, int32_t) {
+  return 0;
+}
+
+minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                                    const minipic_rope* rope, const minipic_prefill_batch* batch, float scale,
+                                    void* workspace, size_t workspace_bytes, minipic_stream_t stream) {
+  (void)num_q_heads;
+  (void)kv;
+  (void)rope;
+  (void)batch;
+  (void)scale;
+  (void)workspace;
+  (void)workspace_bytes;
+  (void)stream;
+  if (dtype != MINIPIC_BF16) return MINIPIC_ERR_UNSUPPORTED;
+  return MINIPIC_ERR_UNSUPPORTED;
+}
+
+minipic_status minipic_device_error(int32_t* flags_out, int32_t clear, minipic_stream_t stream) {
+  int* err = nullptr;
+  if (device_info(&err, nullptr) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  if (clear && v) {
+    if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  }
+  if (flags_out) *flags_out = v;
+  return v ? MINIPIC_ERR_DEVICE_CHECK : MINIPIC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace minipic {
+
+// Arguments of one decode launch (built by the C-ABI layer after validation).
+struct DecodeArgs {
+  const void* q;             // [B][Hq][D]
+  const void* k_pool;        // [num_blocks][Hkv][BS][D]
+  const void* v_pool;
+  const int32_t* block_tables;
+  const int32_t* block_starts;
+  const int32_t* seq_lens;
+  const int32_t* q_pos;
+  const float* cos_sin;      // [max_pos][D] or null when rotation is compiled out
+  int max_pos;
+  void* out;                 // [B][Hq][D]
+  float* lse;                // [B][Hq] or null
+  float* part_o;             // [B][Hq][n_split][D] (unnormalised), null when n_split == 1
+  float* part_ml;            // [B][Hq][n_split][2] (max, sum) in log2 units
+  int batch, Hq, Hkv, G, D, BS, num_blocks, max_blocks;
+  int split_blocks;          // blocks per split
+  int n_split;               // splits per (request, kv head)
+  float scale;               // softmax scale (1/sqrt(D) by default)
+  int* err;                  // device error word
+};
+
+// Arguments of one prefill launch.
+struct PrefillArgs {
+  const void* q;             // [total_q][Hq][D]
+  const int32_t* cu_q_lens;  // [B+1]
+  const int32_t* q_pos;      // [total_q]
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_tables;
+  const int32_t* block_starts;
+  const int32_t* kv_lens;
+  const float* cos_sin;
+  int max_pos;
+  void* out;
+  float* lse;
+  int batch, total_q, max_q_len, Hq, Hkv, G, D, BS, num_blocks, max_blocks;
+  float scale;
+  int* err;
+};
+
+// Error bits (mirror MINIPIC_DEVERR_* of the public header).
+enum : int { kErrBlockId = 1, kErrPosition = 2, kErrSeqLen = 4 };
+
+// Launchers; return cudaSuccess or the launch error.
+cudaError_t launch_rope_table(float* cos_sin, int max_pos, int head_dim, double base, cudaStream_t s);
+
+// Split planning of the decode kernels (same plan used for workspace sizing).
+struct DecodePlan {
+  int split_blocks;
+  int n_split;
+  bool use_mma;
+};
+DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs, bool bf16, int num_sms);
+
+cudaError_t launch_decode(const DecodeArgs& a, bool bf16, bool rotate, const DecodePlan& plan, cudaStream_t s);
+cudaError_t launch_decode_simt(const DecodeArgs& a, bool bf16, bool rotate, cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeArgs& a, bool rotate, cudaStream_t s);
+cudaError_t launch_decode_merge(const DecodeArgs& a, bool bf16, cudaStream_t s);
+
+}  // namespace minipic

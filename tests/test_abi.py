@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+validation rejects bad arguments before any launch (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import position_independent_kv_paged_gb300 as mp
+from position_independent_kv_paged_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "minipic.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return mp.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(minipic_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("minipic_rope_table", "minipic_attn_decode", "minipic_attn_prefill",
+              "minipic_attn_decode_workspace_size", "minipic_status_string", "minipic_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(mp.library_path())
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    assert lib.minipic_status_string(0) == b"ok"
+    assert b"invalid" in lib.minipic_status_string(1)
+    assert lib.minipic_status_string(99) == b"unknown status"
+
+
+def _kv(nb=4, hkv=2, bs=16, d=128, k=0x1000, v=0x2000):
+    return mp._KV(k, v, nb, hkv, bs, d)
+
+
+def _decode(B=1, mb=4, q=0x3000, bt=0x4000, st=0x5000, sl=0x6000, qp=0x7000, out=0x8000):
+    return mp._Decode(q, bt, st, sl, qp, B, mb, out, None)
+
+
+def _call_decode(lib, dtype=1, Hq=4, kv=None, rope=None, db=None, ws=None, ws_n=0, rope_ok=True):
+    kv = kv or _kv()
+    rope = rope or mp._Rope(0x9000, 1024, kv.head_dim)
+    db = db or _decode()
+    return lib.minipic_attn_decode(dtype, Hq, ctypes.byref(kv), ctypes.byref(rope), ctypes.byref(db),
+                                   0.0, ws, ws_n, None)
+
+
+def test_decode_validation_errors(lib):
+    # fake (never dereferenced) pointers: every case fails validation before any launch
+    assert _call_decode(lib, dtype=7) == 1
+    assert _call_decode(lib, Hq=3) == 1                      # Hq % Hkv != 0
+    assert _call_decode(lib, kv=_kv(d=96)) == 2              # head_dim unsupported
+    assert _call_decode(lib, kv=_kv(bs=32)) == 2             # block size unsupported
+    assert _call_decode(lib, Hq=34, kv=_kv(hkv=2)) == 2      # group of 17 > 16
+    assert _call_decode(lib, kv=_kv(k=0x1001)) == 1          # misaligned pool
+    assert _call_decode(lib, rope=mp._Rope(0x9000, 1024, 64)) == 1   # table head_dim mismatch
+    assert _call_decode(lib, rope=mp._Rope(0, 1024, 128)) == 1       # null table
+    assert _call_decode(lib, rope=mp._Rope(0x9000, 0, 128)) == 1     # empty table
+    assert _call_decode(lib, db=_decode(q=0)) == 1                   # null q
+    assert _call_decode(lib, db=_decode(mb=0)) == 1                  # no table width
+    assert _call_decode(lib, db=_decode(out=0x8004)) == 1            # misaligned out
+    assert _call_decode(lib, db=_decode(B=-1)) == 1
+    # batch 0 is a no-op
+    assert _call_decode(lib, db=_decode(B=0)) == 0
+
+
+def test_rope_table_validation(lib):
+    assert lib.minipic_rope_table(None, 10, 64, 1e4, None) == 1
+    assert lib.minipic_rope_table(0x1000, 0, 64, 1e4, None) == 1
+    assert lib.minipic_rope_table(0x1000, 10, 63, 1e4, None) == 1
+    assert lib.minipic_rope_table(0x1000, 10, 64, -1.0, None) == 1
+    assert lib.minipic_rope_table(0x1004, 10, 64, 1e4, None) == 1
+
+
+def test_prefill_rejects_f32(lib):
+    kv = _kv()
+    rope = mp._Rope(0x9000, 1024, 128)
+    pb = mp._Prefill(0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000, 1, 16, 16, 4, 0xA000, None)
+    assert lib.minipic_attn_prefill(0, 4, ctypes.byref(kv), ctypes.byref(rope), ctypes.byref(pb),
+                                    0.0, None, 0, None) == 2
+
+
+def test_workspace_size_is_pure_host(lib):
+    n = lib.minipic_attn_decode_workspace_size(8, 64, 8, 128, 8192, 16)
+    assert n >= 0
+    assert lib.minipic_attn_decode_workspace_size(0, 64, 8, 128, 8192, 16) == 0

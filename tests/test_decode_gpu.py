@@ -1,0 +1,184 @@
+"""Decode parity: the CUDA path (through the C ABI) against the CPU oracle."""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import TOL, compare, compare_lse, upload_decode, to_dev, i32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from position_independent_kv_paged_gb300 import _build
+    _build.build()
+    import position_independent_kv_paged_gb300 as mp
+    mp.load()
+    return torch, mp, torch.device("cuda:0")
+
+
+def run_decode(env, w, prerotated=False, t=None, rope=None):
+    torch, mp, dev = env
+    t = t or upload_decode(w, torch, dev)
+    lse = torch.full((w.decode.batch, w.Hq), float("nan"), dtype=torch.float32, device=dev)
+    if prerotated:
+        out, _ = mp.attn_decode_prerotated(t["q"], t["k_pool"], t["v_pool"], t["block_tables"],
+                                           t["block_starts"], t["seq_lens"], t["q_pos"], lse=lse)
+    else:
+        rope = rope if rope is not None else mp.rope_table(w.max_pos, w.d, w.rope_base, device=dev)
+        out, _ = mp.attn_decode(t["q"], t["k_pool"], t["v_pool"], t["block_tables"], t["block_starts"],
+                                t["seq_lens"], t["q_pos"], rope, lse=lse)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("d,base,max_pos", [(64, 10000.0, 129), (128, 500000.0, 131073), (128, 1e6, 32769)])
+def test_rope_table_within_one_ulp(env, d, base, max_pos):
+    torch, mp, dev = env
+    T = mp.rope_table(max_pos, d, base, device=dev).cpu().numpy().astype(np.float64)
+    R = oracle.rope_table(max_pos, d, base)
+    ulp = np.spacing(np.abs(R).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(T - R) <= ulp + 1e-30)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiny_decode(env, dtype):
+    w = W.tiny_decode(0, dtype)
+    out, lse = run_decode(env, w)
+    ref, rl = oracle.decode(w)
+    compare(out, ref, dtype, "tiny_decode")
+    compare_lse(lse, rl, dtype, "tiny_decode")
+    assert env[1].device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rag_decode_scaled(env, dtype):
+    w = W.rag_decode(1, dtype, B=3, n_spans=6, span_tokens=256, pool_spans=16, tail_tokens=77)
+    out, lse = run_decode(env, w)
+    ref, rl = oracle.decode(w)
+    compare(out, ref, dtype, "rag_decode small")
+    compare_lse(lse, rl, dtype, "rag_decode small")
+
+
+def test_long_decode_scaled(env):
+    w = W.long_decode(2, "bf16", B=2, n_spans=6, span_tokens=4096, pool_spans=5)
+    out, lse = run_decode(env, w)
+    ref, rl = oracle.decode(w)
+    compare(out, ref, "bf16", "long_decode small")
+    compare_lse(lse, rl, "bf16", "long_decode small")
+
+
+def test_mixed_decode_part_scaled(env):
+    w = W.mixed_batch(3, n_prefill=0, n_decode=6, min_ctx=1, max_ctx=3000)
+    out, lse = run_decode(env, w)
+    ref, rl = oracle.decode(w)
+    compare(out, ref, "bf16", "mixed decodes")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 8, 128), (6, 2, 64), (28, 4, 128), (32, 2, 128), (16, 1, 64)])
+def test_irregular_positions_ragged_lengths(env, dtype, Hq, Hkv, d):
+    w = W.irregular_decode(11 + Hq, dtype, seq_lens=[0, 1, 15, 16, 17, 250, 1000], Hq=Hq, Hkv=Hkv, d=d,
+                           max_pos=70000)
+    out, lse = run_decode(env, w)
+    ref, rl = oracle.decode(w)
+    compare(out, ref, dtype, f"irregular {Hq}/{Hkv}/{d}")
+    compare_lse(lse, rl, dtype, "irregular")
+    assert np.all(out[0] == 0.0) and np.all(np.isneginf(lse[0]))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_single_key_returns_value_row_bit_exact(env, dtype):
+    w = W.irregular_decode(21, dtype, seq_lens=[1] * 9, Hq=8, Hkv=2, d=128, max_pos=100000)
+    out, _ = run_decode(env, w)
+    dec = w.decode
+    for r in range(dec.batch):
+        for h in range(w.Hq):
+            row = w.kv.v_pool[dec.block_tables[r, 0], h // 4, 0]
+            exp = W.bf16_bits_to_f32(row) if dtype == "bf16" else row
+            assert np.array_equal(out[r, h].astype(np.float32), exp)
+
+
+def test_zero_query_gives_mean_of_gathered_values(env):
+    w = W.irregular_decode(22, "f32", seq_lens=[37, 300], Hq=4, Hkv=2, d=128, max_pos=5000)
+    w.decode.q[:] = 0.0
+    out, lse = run_decode(env, w)
+    dec = w.decode
+    for r in range(dec.batch):
+        phys, slot, _ = oracle.key_index_map(dec.block_tables[r], dec.block_starts[r], int(dec.seq_lens[r]), 16)
+        for h in range(w.Hq):
+            mean = w.kv.v_pool[phys, h // 2, slot].astype(np.float64).mean(0)
+            assert np.abs(out[r, h] - mean).max() < 1e-5
+            assert abs(lse[r, h] - np.log(dec.seq_lens[r])) < 1e-5
+
+
+def test_split_invariance(env):
+    """A request decoded alone (many splits) equals the same request inside a
+    large batch (fewer splits)."""
+    w = W.long_decode(4, "bf16", B=24, n_spans=1, span_tokens=4096, pool_spans=3)
+    out_b, _ = run_decode(env, w)
+    w1 = W.long_decode(4, "bf16", B=24, n_spans=1, span_tokens=4096, pool_spans=3)
+    d = w1.decode
+    w1.decode = W.DecodeBatch(d.q[:1], d.block_tables[:1], d.block_starts[:1], d.seq_lens[:1], d.q_pos[:1])
+    out_1, _ = run_decode(env, w1)
+    assert np.abs(out_1[0] - out_b[0]).max() <= 2e-3
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prerotated_variant_equals_oracle_on_private_copies(env, dtype):
+    """The rotation-free kernel over a cache pre-rotated on the host (each
+    block used at one offset only) equals the oracle over the unrotated cache."""
+    w = W.rag_decode(5, dtype, B=3, n_spans=4, span_tokens=128, pool_spans=8, tail_tokens=40, share=False)
+    ref, rl = oracle.decode(w)
+    dec = w.decode
+    k = oracle.widen(w.kv.k_pool, dtype).copy()
+    for r in range(dec.batch):
+        phys, slot, pos = oracle.key_index_map(dec.block_tables[r], dec.block_starts[r], int(dec.seq_lens[r]), 16)
+        for g in range(w.Hkv):
+            k[phys, g, slot] = oracle.rope_rotate(k[phys, g, slot], pos, w.rope_base)
+    q = np.stack([oracle.rope_rotate(oracle.widen(dec.q[r], dtype), [int(dec.q_pos[r])] * w.Hq, w.rope_base)
+                  for r in range(dec.batch)])
+    store = (lambda a: W.to_bf16_bits(a.astype(np.float32))) if dtype == "bf16" else (lambda a: a.astype(np.float32))
+    w.kv.k_pool = store(k)
+    w.decode.q = store(q)
+    out, lse = run_decode(env, w, prerotated=True)
+    compare(out, ref, dtype, "prerotated")
+
+
+def test_device_checks_flag_bad_block_ids_and_positions(env):
+    torch, mp, dev = env
+    w = W.irregular_decode(30, "bf16", seq_lens=[40, 40, 40], Hq=4, Hkv=2, d=128, max_pos=1000)
+    mp.device_error(clear=True)
+    w.decode.block_tables[0, 1] = w.kv.k_pool.shape[0] + 5    # block id past the pool
+    run_decode(env, w)
+    assert mp.device_error(clear=True) & 1
+    w = W.irregular_decode(30, "bf16", seq_lens=[40, 40, 40], Hq=4, Hkv=2, d=128, max_pos=1000)
+    w.decode.block_starts[1, 0] = 5000                          # position past the table
+    run_decode(env, w)
+    assert mp.device_error(clear=True) & 2
+    w = W.irregular_decode(30, "bf16", seq_lens=[40, 40, 40], Hq=4, Hkv=2, d=128, max_pos=1000)
+    w.decode.seq_lens[2] = 10 ** 6                              # longer than the table row
+    run_decode(env, w)
+    assert mp.device_error(clear=True) & 4
+    assert mp.device_error(clear=True) == 0
+
+
+# ---------------------------------------------------------------- full sizes (sampled outputs)
+
+@pytest.mark.parametrize("idx,sample", [(1, [0, 31, 63]), (3, [2]), (4, [0, 77, 127])])
+def test_full_size_decode_sampled(env, idx, sample):
+    torch, mp, dev = env
+    w = W.config(idx)
+    if idx == 4:
+        w.prefill = None
+    out, lse = run_decode(env, w)
+    ref, rl = oracle.decode(w, requests=sample)
+    compare(out[sample], ref[sample], "bf16", f"config {idx} sampled")
+    compare_lse(lse[sample], rl[sample], "bf16", f"config {idx} sampled")
+    assert np.all(np.isfinite(out))
+    assert mp.device_error() == 0
