@@ -83,6 +83,7 @@ typedef enum { MINIPIC_F32 = 0, MINIPIC_BF16 = 1 } minipic_dtype;
 #define MINIPIC_DEVERR_BLOCK_ID   1  /* a block table entry outside [0, num_blocks) */
 #define MINIPIC_DEVERR_POSITION   2  /* a key or query position outside [0, max_pos) */
 #define MINIPIC_DEVERR_SEQ_LEN    4  /* a length above max_blocks_per_seq * block_size or negative */
+#define MINIPIC_DEVERR_TIMEOUT    8  /* a bounded wait for an asynchronous copy gave up (results invalid) */
 
 /* The paged KV pool (device memory, caller-owned). */
 typedef struct {

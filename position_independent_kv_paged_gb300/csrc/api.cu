@@ -153,19 +153,31 @@ minipic_status decode_common(minipic_dtype dtype, int32_t num_q_heads, const min
 }  // namespace
 
 DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs, bool bf16, int num_sms) {
-  (void)G;
   (void)D;
   (void)bs;
-  (void)bf16;
-  DecodePlan p{max_blocks, 1, false};
+  DecodePlan p{max_blocks, 1, bf16};
   const long long pairs = (long long)batch * Hkv;
-  const long long target = (long long)num_sms * 4;
-  const int min_split_blocks = 8;
-  if (pairs >= target || max_blocks <= min_split_blocks) return p;
-  long long n = (target + pairs - 1) / pairs;
-  const long long cap = (max_blocks + min_split_blocks - 1) / min_split_blocks;
-  if (n > cap) n = cap;
-  if (n < 1) n = 1;
+  if (!bf16) {
+    // SIMT path: aim for ~4 CTAs per SM, splits of at least 8 blocks
+    const long long target = (long long)num_sms * 4;
+    const int min_split_blocks = 8;
+    if (pairs >= target || max_blocks <= min_split_blocks) return p;
+    long long n = (target + pairs - 1) / pairs;
+    const long long cap = (max_blocks + min_split_blocks - 1) / min_split_blocks;
+    if (n > cap) n = cap;
+    if (n < 1) n = 1;
+    p.split_blocks = (int)((max_blocks + n - 1) / n);
+    p.n_split = (max_blocks + p.split_blocks - 1) / p.split_blocks;
+    return p;
+  }
+  // tensor-core path: CTAs of 4 warps, 2 resident per SM (1 for groups > 8);
+  // ~12 waves of CTAs, each split at least 32 blocks (8 per warp)
+  const long long resident = (long long)num_sms * (G <= 8 ? 2 : 1);
+  const long long total = pairs * max_blocks;
+  long long est = (total + resident * 12 - 1) / (resident * 12);
+  if (est < 32) est = 32;
+  if (est >= max_blocks) return p;
+  const long long n = (max_blocks + est - 1) / est;
   p.split_blocks = (int)((max_blocks + n - 1) / n);
   p.n_split = (max_blocks + p.split_blocks - 1) / p.split_blocks;
   return p;
@@ -173,8 +185,7 @@ DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs,
 
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, bool rotate, const DecodePlan& plan,
                           cudaStream_t s) {
-  (void)plan;
-  cudaError_t e = launch_decode_simt(a, bf16, rotate, s);
+  cudaError_t e = plan.use_mma ? launch_decode_mma(a, rotate, s) : launch_decode_simt(a, bf16, rotate, s);
   if (e != cudaSuccess) return e;
   return launch_decode_merge(a, bf16, s);
 }

@@ -1,0 +1,540 @@
+// Decode attention over the position-free paged cache, bf16 tensor-core form.
+//
+// Method (MiniPIC summary, gist.science 2606.13126, section 2.1): keys are
+// stored unrotated; the kernel rotates them at their logical position
+// pi(j) = start[r][block] + slot with a cos/sin table lookup and multiply-adds
+// per key element, then runs ordinary softmax attention.
+//
+// Layout of the work.  One CTA = (split, kv head, request); each of its 4 warps
+// owns every 4th block of the split and runs its own 3-stage TMA pipeline: the
+// (block, head) K and V tiles (16 keys x d, contiguous in the pool) arrive by
+// cp.async.bulk.tensor with 128-byte swizzle, in a [half][key][64] shared
+// layout that makes both the 16-byte key-row reads and the transposing
+// ldmatrix reads of V free of bank conflicts.
+//
+// Per 16-key block and GQA group (up to 8 query heads per n-tile):
+//   S^T[key][head] = K'[key][:] . Q'[head][:]  (mma m16n8k16, M = the 16 keys)
+//   O^T[dim][head] += V^T[dim][key] P^T[key][head]
+// K' is formed in registers: rows are read from shared memory, rotated in
+// fp32 with two multiply-adds per element, and packed to bf16 as the MMA's A
+// operand.  The contraction order of the head dimension is a per-thread
+// permutation chosen so that each rotary pair (i, i + d/2) is thread-local;
+// Q' uses the same permutation.
+//
+// Rotation is factored per block: with s = slot and b = block start,
+//   (R_t q)^T (R_{b+s} k~) = (R_{t-b} q)^T (R_s k~),
+// so q is re-rotated once per block by the table row |t - b| (sin negated for
+// t < b) and each key row by the constant R_s (s < 16) held in registers.
+// This is the same algebra as rotating k~ by R_{pi(j)}; it reads one 512-byte
+// table row per block instead of sixteen.
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace minipic {
+namespace {
+
+using ptx::U4;
+
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct Geo {
+  static constexpr int TILE = 16 * D * 2;     // bytes of one (block, head) tile of K or V
+  static constexpr int NCH = D / 32;          // 16-byte chunks of a key row read by one thread
+  static constexpr int NPAIR = NCH / 2;       // rotary chunk pairs per row and thread
+  static constexpr int MT = D / 16;           // m-tiles of O^T
+  static constexpr int HALVES = D / 64;       // 128-byte halves of a key row
+  static constexpr int STAGE = 2 * TILE;
+};
+
+// Which 16-byte chunk (0..7 within a 128-byte half) and which half thread
+// `tig` reads as its i-th chunk of a key row, and the rotary pairing.
+template <int D>
+struct Chunks {
+  int c[Geo<D>::NCH];
+  int h[Geo<D>::NCH];
+  int first[Geo<D>::NPAIR], second[Geo<D>::NPAIR];
+  int fbase[Geo<D>::NPAIR];  // first frequency index of the pair's 8 elements
+  float sigma;               // +1, or -1 when `first` holds the upper element of the pair
+  __device__ __forceinline__ explicit Chunks(int tig) {
+    if constexpr (D == 128) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        h[i] = i >> 1;
+        c[i] = 2 * tig + (i & 1);
+      }
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        first[p] = p;
+        second[p] = p + 2;
+        fbase[p] = 8 * (2 * tig + p);
+      }
+      sigma = 1.f;
+    } else {
+      const int c0 = (0x7520 >> (4 * tig)) & 0xf;  // 0, 2, 5, 7
+      c[0] = c0;
+      c[1] = c0 ^ 4;
+      h[0] = h[1] = 0;
+      first[0] = 0;
+      second[0] = 1;
+      fbase[0] = 8 * (c0 & 3);
+      sigma = c0 < 4 ? 1.f : -1.f;
+    }
+  }
+};
+
+// Byte offset of (half, key, chunk) in a swizzled [half][16 keys][128 B] tile.
+__device__ __forceinline__ uint32_t swz(int half, int key, int chunk) {
+  return (uint32_t)((half * 16 + key) * 128 + ((chunk ^ (key & 7)) << 4));
+}
+
+// Rotate one pair of 8-element bf16 chunks in fp32 and repack:
+//   x' = x c - y s,  y' = y c + x s   (c, s already carry sign and scale)
+__device__ __forceinline__ void rotate_pair(U4& x, U4& y, const float (&c)[8], const float (&s)[8]) {
+  uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+  uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float x0 = ptx::bf_lo(xw[k]), x1 = ptx::bf_hi(xw[k]);
+    const float y0 = ptx::bf_lo(yw[k]), y1 = ptx::bf_hi(yw[k]);
+    const float c0 = c[2 * k], c1 = c[2 * k + 1], s0 = s[2 * k], s1 = s[2 * k + 1];
+    xw[k] = ptx::pack_bf16(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
+    yw[k] = ptx::pack_bf16(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+  }
+  x = U4{xw[0], xw[1], xw[2], xw[3]};
+  y = U4{yw[0], yw[1], yw[2], yw[3]};
+}
+
+__device__ __forceinline__ U4 scale_chunk(const U4& x, float f) {
+  return U4{ptx::pack_bf16(ptx::bf_lo(x.x) * f, ptx::bf_hi(x.x) * f),
+            ptx::pack_bf16(ptx::bf_lo(x.y) * f, ptx::bf_hi(x.y) * f),
+            ptx::pack_bf16(ptx::bf_lo(x.z) * f, ptx::bf_hi(x.z) * f),
+            ptx::pack_bf16(ptx::bf_lo(x.w) * f, ptx::bf_hi(x.w) * f)};
+}
+
+__device__ __forceinline__ uint32_t w_of(const U4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+template <int D, int NT, bool ROPE>
+__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      const DecodeArgs a) {
+  using GE = Geo<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - ptx::smem_addr(smem_raw));
+  const uint32_t bar_base = sbase + kWarps * kStages * GE::STAGE;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g8 = lane >> 2, tig = lane & 3;
+  const int split = blockIdx.x, hk = blockIdx.y, r = blockIdx.z;
+  const int G = a.G;
+  const int mb = a.max_blocks;
+
+  int L = a.seq_lens[r];
+  const int Lmax = mb * 16;
+  if (L < 0 || L > Lmax) {
+    if (threadIdx.x == 0 && split == 0) atomicOr(a.err, kErrSeqLen);
+    L = L < 0 ? 0 : Lmax;
+  }
+  const int nblk = (L + 15) >> 4;
+  const int n_valid = max(1, (nblk + a.split_blocks - 1) / a.split_blocks);
+  if (split >= n_valid) return;
+  const int b_begin = split * a.split_blocks;
+  const int b_end = min(nblk, b_begin + a.split_blocks);
+  const int span = b_end - b_begin;
+  const int nmine = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) ptx::mbar_init(bar_base + (warp * kStages + st) * 8, 1);
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+  }
+  __syncwarp();
+
+  const Chunks<D> ch(tig);
+
+  // unrotated queries of this thread's heads (g8 + 8 nt), in the thread's chunk order
+  U4 qraw[NT][GE::NCH];
+  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int head = 8 * nt + g8;
+#pragma unroll
+    for (int i = 0; i < GE::NCH; ++i) {
+      if (head < G) {
+        const __nv_bfloat16* p = qg + ((size_t)r * a.Hq + (size_t)hk * G + head) * D + 64 * ch.h[i] + 8 * ch.c[i];
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+        qraw[nt][i] = U4{v.x, v.y, v.z, v.w};
+      } else {
+        qraw[nt][i] = U4{0u, 0u, 0u, 0u};
+      }
+    }
+  }
+  const float qs = a.scale * kLog2e;  // softmax runs in base 2
+
+  // R_s for the two key rows (slots g8, g8 + 8) of this thread
+  float rsc[2][GE::NPAIR][8], rss[2][GE::NPAIR][8];
+  int tq = 0;
+  if constexpr (ROPE) {
+#pragma unroll
+    for (int row = 0; row < 2; ++row) {
+      const int srow = min(g8 + 8 * row, a.max_pos - 1);
+      const float* t = a.cos_sin + (size_t)srow * D;
+#pragma unroll
+      for (int p = 0; p < GE::NPAIR; ++p) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          rsc[row][p][e] = __ldg(t + ch.fbase[p] + e);
+          rss[row][p][e] = ch.sigma * __ldg(t + D / 2 + ch.fbase[p] + e);
+        }
+      }
+    }
+    tq = a.q_pos[r];
+    if (tq < 0 || tq >= a.max_pos) {
+      if (threadIdx.x == 0 && split == 0) atomicOr(a.err, kErrPosition);
+      tq = 0;
+    }
+  }
+  U4 qw[NT][GE::NCH];
+  if constexpr (!ROPE) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < GE::NCH; ++i) qw[nt][i] = scale_chunk(qraw[nt][i], qs);
+  }
+
+  float mrun[NT][2], lrun[NT][2];
+  float oacc[GE::MT][NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    mrun[nt][0] = mrun[nt][1] = -CUDART_INF_F;
+    lrun[nt][0] = lrun[nt][1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < GE::MT; ++mt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) oacc[mt][nt][k] = 0.f;
+  }
+
+  const int* bt = a.block_tables + (size_t)r * mb;
+  const int* bs_ = a.block_starts + (size_t)r * mb;
+
+  // lane 0: issue the k-th block of this warp into its stage
+  auto issue = [&](int k) {
+    const int b = b_begin + warp + kWarps * k;
+    const int stg = k % kStages;
+    const uint32_t bar = bar_base + (warp * kStages + stg) * 8;
+    const uint32_t kdst = sbase + (warp * kStages + stg) * GE::STAGE;
+    const int phys = __ldg(bt + b);
+    if (phys < 0 || phys >= a.num_blocks) {
+      ptx::mbar_arrive(bar);  // nothing to load; the consumer masks the block
+      return;
+    }
+    ptx::mbar_arrive_expect_tx(bar, 2 * GE::TILE);
+    const int y = (phys * a.Hkv + hk) * 16;
+#pragma unroll
+    for (int hh = 0; hh < GE::HALVES; ++hh) {
+      ptx::tma_load_2d(kdst + hh * 2048, &kmap, 64 * hh, y, bar);
+      ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
+    }
+  };
+  if (lane == 0) {
+    const int pre = nmine < kStages ? nmine : kStages;
+    for (int k = 0; k < pre; ++k) issue(k);
+  }
+
+  bool timed_out = false;
+  int k_stop = nmine;
+  for (int k = 0; k < nmine; ++k) {
+    const int b = b_begin + warp + kWarps * k;
+    const int stg = k % kStages;
+    const uint32_t bar = bar_base + (warp * kStages + stg) * 8;
+    const uint32_t kbase = sbase + (warp * kStages + stg) * GE::STAGE;
+    const uint32_t vbase = kbase + GE::TILE;
+
+    const int phys = __ldg(bt + b);
+    const bool ok = phys >= 0 && phys < a.num_blocks;
+    const int start = ROPE ? __ldg(bs_ + b) : 0;
+    const int nk = min(16, L - b * 16);
+    bool v0 = ok && g8 < nk, v1 = ok && g8 + 8 < nk;
+    if (!ok && lane == 0) atomicOr(a.err, kErrBlockId);
+
+    // re-rotate q by t - start (overlaps the wait for the tiles)
+    if constexpr (ROPE) {
+      const int delta = tq - start;
+      const int ad = delta < 0 ? -delta : delta;
+      const bool pos_ok = ad < a.max_pos && start >= 0 && start + nk - 1 < a.max_pos;
+      const int arow = ad < a.max_pos ? ad : 0;
+      if (ok && !pos_ok) {
+        // keys whose position falls outside the table are masked
+        const bool p0 = start + g8 >= 0 && start + g8 < a.max_pos && ad < a.max_pos;
+        const bool p1 = start + g8 + 8 >= 0 && start + g8 + 8 < a.max_pos && ad < a.max_pos;
+        if (__any_sync(0xffffffffu, (v0 && !p0) || (v1 && !p1)) && lane == 0) atomicOr(a.err, kErrPosition);
+        v0 = v0 && p0;
+        v1 = v1 && p1;
+      }
+      const float* trow = a.cos_sin + (size_t)arow * D;
+      const float sg = (delta < 0 ? -ch.sigma : ch.sigma) * qs;
+#pragma unroll
+      for (int p = 0; p < GE::NPAIR; ++p) {
+        float c[8], s[8];
+        const float4 c0 = __ldg(reinterpret_cast<const float4*>(trow + ch.fbase[p]));
+        const float4 c1 = __ldg(reinterpret_cast<const float4*>(trow + ch.fbase[p] + 4));
+        const float4 s0 = __ldg(reinterpret_cast<const float4*>(trow + D / 2 + ch.fbase[p]));
+        const float4 s1 = __ldg(reinterpret_cast<const float4*>(trow + D / 2 + ch.fbase[p] + 4));
+        c[0] = c0.x * qs; c[1] = c0.y * qs; c[2] = c0.z * qs; c[3] = c0.w * qs;
+        c[4] = c1.x * qs; c[5] = c1.y * qs; c[6] = c1.z * qs; c[7] = c1.w * qs;
+        s[0] = s0.x * sg; s[1] = s0.y * sg; s[2] = s0.z * sg; s[3] = s0.w * sg;
+        s[4] = s1.x * sg; s[5] = s1.y * sg; s[6] = s1.z * sg; s[7] = s1.w * sg;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          U4 x = qraw[nt][ch.first[p]], y = qraw[nt][ch.second[p]];
+          rotate_pair(x, y, c, s);
+          qw[nt][ch.first[p]] = x;
+          qw[nt][ch.second[p]] = y;
+        }
+      }
+    }
+
+    // wait for this block's tiles (bounded)
+    const bool arrived = ptx::mbar_wait(bar, (uint32_t)((k / kStages) & 1));
+    if (!__all_sync(0xffffffffu, arrived)) {
+      if (lane == 0) atomicOr(a.err, kErrTimeout);
+      timed_out = true;
+      k_stop = k;
+      break;
+    }
+
+    // key rows g8 and g8 + 8 of the block, rotated by R_slot in registers
+    U4 kr[2][GE::NCH];
+#pragma unroll
+    for (int row = 0; row < 2; ++row)
+#pragma unroll
+      for (int i = 0; i < GE::NCH; ++i) kr[row][i] = ptx::lds128(kbase + swz(ch.h[i], g8 + 8 * row, ch.c[i]));
+    if constexpr (ROPE) {
+#pragma unroll
+      for (int row = 0; row < 2; ++row)
+#pragma unroll
+        for (int p = 0; p < GE::NPAIR; ++p) rotate_pair(kr[row][ch.first[p]], kr[row][ch.second[p]], rsc[row][p], rss[row][p]);
+    }
+
+    // S^T = K' Q'^T
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < GE::NCH; ++i) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t a0 = w_of(kr[0][i], 2 * u), a1 = w_of(kr[1][i], 2 * u);
+        const uint32_t a2 = w_of(kr[0][i], 2 * u + 1), a3 = w_of(kr[1][i], 2 * u + 1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          ptx::mma_bf16_16816(sacc[nt], a0, a1, a2, a3, w_of(qw[nt][i], 2 * u), w_of(qw[nt][i], 2 * u + 1));
+      }
+    }
+
+    // online softmax over the 16 keys, per head column (2 tig + j) of each n-tile
+    uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float pv[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float sa = v0 ? sacc[nt][j] : -CUDART_INF_F;
+        const float sb = v1 ? sacc[nt][2 + j] : -CUDART_INF_F;
+        float bm = fmaxf(sa, sb);
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        const float mnew = fmaxf(mrun[nt][j], bm);
+        const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
+        const float corr = exp2f(mrun[nt][j] - muse);
+        const float pa = exp2f(sa - muse), pbv = exp2f(sb - muse);
+        lrun[nt][j] = fmaf(lrun[nt][j], corr, pa + pbv);
+        mrun[nt][j] = mnew;
+#pragma unroll
+        for (int mt = 0; mt < GE::MT; ++mt) {
+          oacc[mt][nt][j] *= corr;
+          oacc[mt][nt][2 + j] *= corr;
+        }
+        pv[j] = pa;
+        pv[2 + j] = pbv;
+      }
+      pb0[nt] = ptx::movmatrix_trans(ptx::pack_bf16(pv[0], pv[1]));  // keys 0..7
+      pb1[nt] = ptx::movmatrix_trans(ptx::pack_bf16(pv[2], pv[3]));  // keys 8..15
+    }
+
+    // O^T += V^T P^T
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int key = rr + 8 * (mi >> 1);
+#pragma unroll
+      for (int mt = 0; mt < GE::MT; ++mt) {
+        const int cg = 2 * mt + (mi & 1);
+        uint32_t a0, a1, a2, a3;
+        ptx::ldsm_x4_trans(vbase + swz(cg >> 3, key, cg & 7), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) ptx::mma_bf16_16816(oacc[mt][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+      }
+    }
+
+    __syncwarp();
+    if (lane == 0 && k + kStages < nmine) issue(k + kStages);
+  }
+
+  if (timed_out) {
+    // let copies already issued land before the CTA exits (bounded)
+    // blocks k_stop .. k_stop + kStages - 1 were issued and not consumed
+    if (lane == 0) {
+      const int last = min(nmine, k_stop + kStages);
+      for (int k2 = k_stop; k2 < last; ++k2) {
+        const int stg = k2 % kStages;
+        ptx::mbar_wait(bar_base + (warp * kStages + stg) * 8, (uint32_t)((k2 / kStages) & 1), 100000000ull);
+      }
+    }
+  }
+
+  // per-warp state -> this warp's own stage region: m[16], l[16], O[16][D]
+  float* wm = reinterpret_cast<float*>(sgen + warp * kStages * GE::STAGE);
+  float* wl = wm + 16;
+  float* wo = wm + 32;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float l = lrun[nt][j];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      lrun[nt][j] = l;
+    }
+  __syncwarp();
+  if (g8 == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        wm[8 * nt + 2 * tig + j] = mrun[nt][j];
+        wl[8 * nt + 2 * tig + j] = lrun[nt][j];
+      }
+  }
+#pragma unroll
+  for (int mt = 0; mt < GE::MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int head = 8 * nt + 2 * tig + j;
+        wo[head * D + 16 * mt + g8] = oacc[mt][nt][j];
+        wo[head * D + 16 * mt + g8 + 8] = oacc[mt][nt][2 + j];
+      }
+  __syncthreads();
+
+  const bool direct = (n_valid == 1);
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int head = idx / D, dim = idx - head * D;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(sgen + w * kStages * GE::STAGE)[head]);
+    float Ls = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float* base = reinterpret_cast<const float*>(sgen + w * kStages * GE::STAGE);
+      const float mw = base[head];
+      const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
+      Ls = fmaf(base[16 + head], f, Ls);
+      O = fmaf(base[32 + head * D + dim], f, O);
+    }
+    const int hq = hk * G + head;
+    if (direct) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((size_t)r * a.Hq + hq) * D + dim;
+      *out = __float2bfloat16_rn(Ls > 0.f ? O / Ls : 0.f);
+      if (dim == 0 && a.lse) a.lse[(size_t)r * a.Hq + hq] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
+    } else {
+      const size_t pi = ((size_t)r * a.Hq + hq) * a.n_split + split;
+      a.part_o[pi * D + dim] = O;
+      if (dim == 0) {
+        a.part_ml[pi * 2] = M;
+        a.part_ml[pi * 2 + 1] = Ls;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view [rows = num_blocks * Hkv * 16][D] of a bf16 pool; box = 64 x 16, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* m, const void* base, long long rows, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int NT, bool ROPE>
+cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
+  using GE = Geo<D>;
+  const int smem = kWarps * kStages * GE::STAGE + kWarps * kStages * 8 + 1024;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(decode_mma_kernel<D, NT, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  CUtensorMap km, vm;
+  const long long rows = (long long)a.num_blocks * a.Hkv * 16;
+  if (!make_pool_map(&km, a.k_pool, rows, D) || !make_pool_map(&vm, a.v_pool, rows, D))
+    return cudaErrorInvalidValue;
+  dim3 grid(a.n_split, a.Hkv, a.batch);
+  decode_mma_kernel<D, NT, ROPE><<<grid, kWarps * 32, smem, s>>>(km, vm, a);
+  return cudaGetLastError();
+}
+
+template <int D, bool ROPE>
+cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
+  return a.G <= 8 ? launch_t<D, 1, ROPE>(a, s) : launch_t<D, 2, ROPE>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, bool rotate, cudaStream_t s) {
+  if (a.num_blocks <= 0) return launch_decode_simt(a, true, rotate, s);  // nothing to map; all keys masked
+  if (a.D == 128) return rotate ? launch_d<128, true>(a, s) : launch_d<128, false>(a, s);
+  return rotate ? launch_d<64, true>(a, s) : launch_d<64, false>(a, s);
+}
+
+}  // namespace minipic

@@ -48,7 +48,7 @@ struct PrefillArgs {
 };
 
 // Error bits (mirror MINIPIC_DEVERR_* of the public header).
-enum : int { kErrBlockId = 1, kErrPosition = 2, kErrSeqLen = 4 };
+enum : int { kErrBlockId = 1, kErrPosition = 2, kErrSeqLen = 4, kErrTimeout = 8 };
 
 // Launchers; return cudaSuccess or the launch error.
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, int head_dim, double base, cudaStream_t s);
