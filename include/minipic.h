@@ -178,6 +178,28 @@ minipic_status minipic_attn_decode_prerotated(minipic_dtype dtype, int32_t num_q
                                               void* workspace, size_t workspace_bytes,
                                               minipic_stream_t stream);
 
+/* Decode for callers that cannot allocate device memory at the call: code
+ * inside a fixed memory pool that must not grow, a serving loop where an
+ * allocation could synchronize the device or fail under fragmentation, or a
+ * plain C host with no device allocator of its own.  The paper has no
+ * counterpart; this is a deployment convenience.  Same computation, arguments
+ * and errors as minipic_attn_decode, except that the split-KV partial results
+ * go to a fixed device array inside the library (MINIPIC_NOALLOC_SCRATCH_BYTES,
+ * held on every GPU that loads the library until the process exits) instead of
+ * a caller workspace.  Nothing is allocated by this call.
+ *  - Shapes whose partial results exceed the fixed array (as reported by
+ *    minipic_attn_decode_workspace_size) return MINIPIC_ERR_WORKSPACE.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents (no part of it needs to start at zero).  Calls whose work
+ *    overlaps on the GPU race on it: serialize them. */
+#define MINIPIC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+minipic_status minipic_attn_decode_noalloc(minipic_dtype dtype, int32_t num_q_heads,
+                                           const minipic_kv_pool* kv, const minipic_rope* rope,
+                                           const minipic_decode_batch* batch, float scale,
+                                           minipic_stream_t stream);
+
 /* Workspace bytes minipic_attn_prefill needs (0 in this build). */
 size_t minipic_attn_prefill_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                            int32_t head_dim, int32_t max_q_len,
