@@ -176,6 +176,74 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------- GPU legs
 
+def kernel_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, only while the kernel
+    source is unchanged since that capture (sha256 recorded beside it)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "position_independent_kv_paged_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    rec = json.load(open(path)).get(workload)
+    if not rec:
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return rec["traffic"] if rec.get("source_sha256") == sha else None
+
+
+class DecodeCase:
+    """A decode workload resident on the GPU, timed through the C ABI."""
+
+    def __init__(self, w, dev, torch, mp):
+        import numpy as np
+        self.w, self.torch, self.mp = w, torch, mp
+        d = w.decode
+
+        def up(a):
+            if w.dtype == "bf16":
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+            return torch.from_numpy(a).to(dev)
+
+        self.kpool, self.vpool, self.q = up(w.kv.k_pool), up(w.kv.v_pool), up(d.q)
+        self.bt = torch.from_numpy(d.block_tables).to(dev)
+        self.st = torch.from_numpy(d.block_starts).to(dev)
+        self.sl = torch.from_numpy(d.seq_lens).to(dev)
+        self.qp = torch.from_numpy(d.q_pos).to(dev)
+        self.rope = mp.rope_table(w.max_pos, w.d, w.rope_base, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(d.batch, w.Hq, dtype=torch.float32, device=dev)
+        self.ws_n = mp.decode_workspace_size(d.batch, w.Hq, w.Hkv, w.d, self.bt.shape[1])
+        self.ws = torch.empty(max(self.ws_n, 1), dtype=torch.uint8, device=dev)
+        self.nbytes = decode_kv_bytes(w)
+
+    def step(self):
+        self.mp.attn_decode(self.q, self.kpool, self.vpool, self.bt, self.st, self.sl, self.qp, self.rope,
+                            out=self.out, lse=self.lse, workspace=self.ws)
+
+    def step_norope(self):
+        self.mp.attn_decode_prerotated(self.q, self.kpool, self.vpool, self.bt, self.st, self.sl, self.qp,
+                                       out=self.out, lse=self.lse, workspace=self.ws)
+
+    @property
+    def launches_per_step(self):
+        return 2 if self.ws_n > 0 else 1
+
+
+def timed(torch, stream, flush, fn, steps):
+    """Per-step CUDA-event times (ms); L2 flushed before every step, outside the events."""
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def run_minipic(args):
     import numpy as np
     import torch
@@ -199,52 +267,17 @@ def run_minipic(args):
         dist.barrier()
     mp.load()
     pk = peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    # the workload: each rank decodes its own batch (weak scaling, no data-path collective)
+    # the headline workload: each rank decodes its own batch (weak scaling, no collective)
     w = W.rag_decode(seed=rank)
     d = w.decode
-
-    def up(a):
-        if w.dtype == "bf16":
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(a).to(dev)
-
-    kpool, vpool = up(w.kv.k_pool), up(w.kv.v_pool)
-    q = up(d.q)
-    bt = torch.from_numpy(d.block_tables).to(dev)
-    st = torch.from_numpy(d.block_starts).to(dev)
-    sl = torch.from_numpy(d.seq_lens).to(dev)
-    qp = torch.from_numpy(d.q_pos).to(dev)
-    rope = mp.rope_table(w.max_pos, w.d, w.rope_base, device=dev)
-    out = torch.empty_like(q)
-    lse = torch.empty(d.batch, w.Hq, dtype=torch.float32, device=dev)
-    ws_n = mp.decode_workspace_size(d.batch, w.Hq, w.Hkv, w.d, bt.shape[1])
-    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-    nbytes = decode_kv_bytes(w)
-
-    def step():
-        mp.attn_decode(q, kpool, vpool, bt, st, sl, qp, rope, out=out, lse=lse, workspace=ws)
-
-    def step_norope():
-        mp.attn_decode_prerotated(q, kpool, vpool, bt, st, sl, qp, out=out, lse=lse, workspace=ws)
-
-    def timed(fn, steps):
-        evs = []
-        for _ in range(steps):
-            flush.zero_()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            evs.append((a, b))
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in evs]
+    case = DecodeCase(w, dev, torch, mp)
+    nbytes = case.nbytes
 
     for _ in range(max(3, args.warmup)):
-        step()
+        case.step()
     torch.cuda.synchronize()
     if mp.device_error() != 0:
         raise RuntimeError("device error during warm-up")
@@ -254,7 +287,7 @@ def run_minipic(args):
     torch.cuda.synchronize()
     with Clocks(local) as clk:
         t_wall = time.perf_counter()
-        ms = timed(step, args.steps)
+        ms = timed(torch, stream, flush, case.step, args.steps)
         t_wall = time.perf_counter() - t_wall
     if dist is not None:
         dist.barrier()
@@ -266,8 +299,6 @@ def run_minipic(args):
         ms_step = float(t.item())
     value = nbytes * world / (ms_step * 1e-3) / 1e9
     achieved = nbytes / (ms_step * 1e-3) / 1e9
-    n_split = (ws_n > 0)
-    kernels_per_step = 2 if n_split else 1
 
     extras = {}
     e2e = None
@@ -275,8 +306,8 @@ def run_minipic(args):
     if not args.no_extras:
         # rotation compiled out, same inputs and memory traffic
         for _ in range(3):
-            step_norope()
-        ms_nr = timed(step_norope, args.steps)
+            case.step_norope()
+        ms_nr = timed(torch, stream, flush, case.step_norope, args.steps)
         ms_nr = sum(ms_nr) / len(ms_nr)
         extras["rope_off"] = {"ms_per_step": ms_nr, "rope_overhead": ms_step / ms_nr - 1.0,
                               "note": "same kernel with rotation compiled out (pre-rotated cache)"}
@@ -286,24 +317,24 @@ def run_minipic(args):
         hst = torch.from_numpy(d.block_starts).pin_memory()
         hsl = torch.from_numpy(d.seq_lens).pin_memory()
         hqp = torch.from_numpy(d.q_pos).pin_memory()
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        hout = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+        hlse = torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hst, hsl, hqp))
         d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
         def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            bt.copy_(hbt, non_blocking=True)
-            st.copy_(hst, non_blocking=True)
-            sl.copy_(hsl, non_blocking=True)
-            qp.copy_(hqp, non_blocking=True)
-            step()
-            hout.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+            case.q.copy_(hq, non_blocking=True)
+            case.bt.copy_(hbt, non_blocking=True)
+            case.st.copy_(hst, non_blocking=True)
+            case.sl.copy_(hsl, non_blocking=True)
+            case.qp.copy_(hqp, non_blocking=True)
+            case.step()
+            hout.copy_(case.out, non_blocking=True)
+            hlse.copy_(case.lse, non_blocking=True)
 
         for _ in range(3):
             e2e_step()
-        ms_e2e = timed(e2e_step, args.steps)
+        ms_e2e = timed(torch, stream, flush, e2e_step, args.steps)
         ms_e2e = sum(ms_e2e) / len(ms_e2e)
         e2e = {"value": nbytes * world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
@@ -312,6 +343,29 @@ def run_minipic(args):
             nb, dt, nreq = oracle_sample(w, args.cpu_seconds)
             cpu = {"value": nb / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                    "sample": f"{nreq} whole request(s) of this batch (numpy float64, single thread), {dt:.1f} s"}
+        del case
+        torch.cuda.empty_cache()
+        # other decode workloads: the no-sharing control and the long-context batch
+        for name, mk in (("no_sharing_control", lambda: W.rag_decode(seed=rank, share=False)),
+                         ("long_decode", lambda: W.long_decode(seed=rank))):
+            wx = mk()
+            cx = DecodeCase(wx, dev, torch, mp)
+            for _ in range(3):
+                cx.step()
+            mx = timed(torch, stream, flush, cx.step, args.steps)
+            mx = sum(mx) / len(mx)
+            for _ in range(3):
+                cx.step_norope()
+            mn = timed(torch, stream, flush, cx.step_norope, args.steps)
+            mn = sum(mn) / len(mn)
+            gbs = cx.nbytes / (mx * 1e-3) / 1e9
+            extras[name] = {"workload": f"{wx.name}: {wx.notes}", "ms_per_step": mx, "GB_s": gbs,
+                            "frac_of_hbm": gbs / pk["hbm"], "rope_off_ms": mn, "rope_overhead": mx / mn - 1.0,
+                            "logical_kv_bytes": cx.nbytes, "unique_kv_bytes": unique_kv_bytes(wx)}
+            if mp.device_error() != 0:
+                raise RuntimeError(f"device error in {name}")
+            del cx, wx
+            torch.cuda.empty_cache()
 
     if rank == 0:
         line = {
@@ -322,11 +376,14 @@ def run_minipic(args):
                            l2=f"flushed before every step by writing {L2_FLUSH_BYTES >> 20} MiB",
                            logical_kv_bytes=nbytes, unique_kv_bytes=unique_kv_bytes(w)),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                         "frac": achieved / pk["hbm"], "traffic": None,
-                         "peak_source": pk["src"], "kernel": "decode (split + merge launches of one call)"},
+                         "frac": achieved / pk["hbm"],
+                         "traffic": kernel_traffic("decode_mma.cu", "rag_decode"),
+                         "peak_source": pk["src"],
+                         "kernel": "decode call (split kernel + log-sum-exp merge kernel)",
+                         "bytes": "logical K+V bytes gathered per request (sum_r L_r * Hkv * d * 2 * 2)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": kernels_per_step * args.steps,
+            "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
             "wall_s_timed": t_wall,
         }

@@ -176,6 +176,7 @@ DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs,
   const long long total = pairs * max_blocks;
   long long est = (total + resident * 12 - 1) / (resident * 12);
   if (est < 32) est = 32;
+  if (est > 512) est = 512;  // the kernel stages a split's block metadata in shared memory
   if (est >= max_blocks) return p;
   const long long n = (max_blocks + est - 1) / est;
   p.split_blocks = (int)((max_blocks + n - 1) / n);

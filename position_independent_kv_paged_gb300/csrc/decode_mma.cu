@@ -56,83 +56,94 @@ struct Geo {
 };
 
 // Which 16-byte chunk (0..7 within a 128-byte half) and which half thread
-// `tig` reads as its i-th chunk of a key row, and the rotary pairing.
+// `tig` reads as its i-th chunk of a key row, and the rotary pairing: thread
+// tig owns chunks tig and tig + 4 of every half, so each rotary pair
+// (i, i + d/2) is thread-local and every shared read below is conflict-free.
 template <int D>
 struct Chunks {
   int c[Geo<D>::NCH];
   int h[Geo<D>::NCH];
   int first[Geo<D>::NPAIR], second[Geo<D>::NPAIR];
   int fbase[Geo<D>::NPAIR];  // first frequency index of the pair's 8 elements
-  float sigma;               // +1, or -1 when `first` holds the upper element of the pair
   __device__ __forceinline__ explicit Chunks(int tig) {
     if constexpr (D == 128) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         h[i] = i >> 1;
-        c[i] = 2 * tig + (i & 1);
+        c[i] = tig + 4 * (i & 1);
       }
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
         first[p] = p;
         second[p] = p + 2;
-        fbase[p] = 8 * (2 * tig + p);
+        fbase[p] = 8 * (tig + 4 * p);
       }
-      sigma = 1.f;
     } else {
-      const int c0 = (0x7520 >> (4 * tig)) & 0xf;  // 0, 2, 5, 7
-      c[0] = c0;
-      c[1] = c0 ^ 4;
+      c[0] = tig;
+      c[1] = tig + 4;
       h[0] = h[1] = 0;
       first[0] = 0;
       second[0] = 1;
-      fbase[0] = 8 * (c0 & 3);
-      sigma = c0 < 4 ? 1.f : -1.f;
+      fbase[0] = 8 * tig;
     }
   }
 };
+
+// Physical key (slot) held by MMA fragment row g (g < 8; row g + 8 holds
+// slot + 8).  Rows read together by a quarter warp then differ in bit 2 of the
+// slot, which keeps the swizzled key-row reads conflict-free.
+__device__ __forceinline__ int frag_slot(int g) { return (g >> 1) | ((g & 1) << 2); }
 
 // Byte offset of (half, key, chunk) in a swizzled [half][16 keys][128 B] tile.
 __device__ __forceinline__ uint32_t swz(int half, int key, int chunk) {
   return (uint32_t)((half * 16 + key) * 128 + ((chunk ^ (key & 7)) << 4));
 }
 
-// Rotate one pair of 8-element bf16 chunks in fp32 and repack:
-//   x' = x c - y s,  y' = y c + x s   (c, s already carry sign and scale)
-__device__ __forceinline__ void rotate_pair(U4& x, U4& y, const float (&c)[8], const float (&s)[8]) {
+// Rotate one pair of 8-element bf16 chunks in fp32 (packed pairs) and repack:
+//   x' = x c - y s,  y' = y c + x s   (s already carries the pair's sign)
+// c2/s2 hold the 8 cosines/sines as 4 packed fp32 pairs.
+__device__ __forceinline__ void rotate_pair(U4& x, U4& y, const uint64_t (&c2)[4], const uint64_t (&s2)[4]) {
   uint32_t xw[4] = {x.x, x.y, x.z, x.w};
   uint32_t yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float x0 = ptx::bf_lo(xw[k]), x1 = ptx::bf_hi(xw[k]);
-    const float y0 = ptx::bf_lo(yw[k]), y1 = ptx::bf_hi(yw[k]);
-    const float c0 = c[2 * k], c1 = c[2 * k + 1], s0 = s[2 * k], s1 = s[2 * k + 1];
-    xw[k] = ptx::pack_bf16(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
-    yw[k] = ptx::pack_bf16(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+    const uint64_t xv = ptx::bf2_to_f2(xw[k]), yv = ptx::bf2_to_f2(yw[k]);
+    const uint64_t xn = ptx::sub2(ptx::mul2(xv, c2[k]), ptx::mul2(yv, s2[k]));
+    const uint64_t yn = ptx::fma2(xv, s2[k], ptx::mul2(yv, c2[k]));
+    xw[k] = ptx::f2_to_bf2(xn);
+    yw[k] = ptx::f2_to_bf2(yn);
   }
   x = U4{xw[0], xw[1], xw[2], xw[3]};
   y = U4{yw[0], yw[1], yw[2], yw[3]};
-}
-
-__device__ __forceinline__ U4 scale_chunk(const U4& x, float f) {
-  return U4{ptx::pack_bf16(ptx::bf_lo(x.x) * f, ptx::bf_hi(x.x) * f),
-            ptx::pack_bf16(ptx::bf_lo(x.y) * f, ptx::bf_hi(x.y) * f),
-            ptx::pack_bf16(ptx::bf_lo(x.z) * f, ptx::bf_hi(x.z) * f),
-            ptx::pack_bf16(ptx::bf_lo(x.w) * f, ptx::bf_hi(x.w) * f)};
 }
 
 __device__ __forceinline__ uint32_t w_of(const U4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
 
+// Shared-memory plan of one CTA (offsets from a 1024-byte aligned base).
+template <int D>
+struct Smem {
+  static constexpr int STAGES = kWarps * kStages * Geo<D>::STAGE;  // K|V tiles
+  static constexpr int ROWB = 4 * D;                               // one cos|sin table row
+  static constexpr int ROWS = STAGES;                              // [warp][stage] table rows
+  static constexpr int META = ROWS + kWarps * kStages * ROWB;      // [split block][phys, start]
+  static constexpr int kMaxSplit = 512;                            // split_blocks cap (planner)
+  static constexpr int BARS = META + kMaxSplit * 8;
+  static constexpr int TOTAL = BARS + kWarps * kStages * 8;
+};
+
 template <int D, int NT, bool ROPE>
 __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const DecodeArgs a) {
   using GE = Geo<D>;
+  using SM = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - ptx::smem_addr(smem_raw));
-  const uint32_t bar_base = sbase + kWarps * kStages * GE::STAGE;
+  const uint32_t bar_base = sbase + SM::BARS;
+  int* meta = reinterpret_cast<int*>(sgen + SM::META);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g8 = lane >> 2, tig = lane & 3;
@@ -154,15 +165,24 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
   const int span = b_end - b_begin;
   const int nmine = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
 
+  // block ids and start positions of the whole split, staged once
+  {
+    const int* bt = a.block_tables + (size_t)r * mb + b_begin;
+    const int* bs_ = a.block_starts + (size_t)r * mb + b_begin;
+    for (int i = threadIdx.x; i < span; i += blockDim.x) {
+      meta[2 * i] = __ldg(bt + i);
+      meta[2 * i + 1] = ROPE ? __ldg(bs_ + i) : 0;
+    }
+  }
   if (lane == 0) {
 #pragma unroll
     for (int st = 0; st < kStages; ++st) ptx::mbar_init(bar_base + (warp * kStages + st) * 8, 1);
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
   }
-  __syncwarp();
 
   const Chunks<D> ch(tig);
+  const int ks0 = frag_slot(g8);  // this thread's key rows: slots ks0 and ks0 + 8
 
   // unrotated queries of this thread's heads (g8 + 8 nt), in the thread's chunk order
   U4 qraw[NT][GE::NCH];
@@ -181,22 +201,24 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
       }
     }
   }
-  const float qs = a.scale * kLog2e;  // softmax runs in base 2
+  const float qs = a.scale * kLog2e;  // applied to the scores; softmax runs in base 2
 
-  // R_s for the two key rows (slots g8, g8 + 8) of this thread
-  float rsc[2][GE::NPAIR][8], rss[2][GE::NPAIR][8];
+  // R_s for the two key rows (slots g8, g8 + 8) of this thread, as packed pairs
+  uint64_t rsc[2][GE::NPAIR][4], rss[2][GE::NPAIR][4];
   int tq = 0;
   if constexpr (ROPE) {
 #pragma unroll
     for (int row = 0; row < 2; ++row) {
-      const int srow = min(g8 + 8 * row, a.max_pos - 1);
+      const int srow = min(ks0 + 8 * row, a.max_pos - 1);
       const float* t = a.cos_sin + (size_t)srow * D;
 #pragma unroll
       for (int p = 0; p < GE::NPAIR; ++p) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          rsc[row][p][e] = __ldg(t + ch.fbase[p] + e);
-          rss[row][p][e] = ch.sigma * __ldg(t + D / 2 + ch.fbase[p] + e);
+        for (int e = 0; e < 4; ++e) {
+          const float2 c = __ldg(reinterpret_cast<const float2*>(t + ch.fbase[p] + 2 * e));
+          const float2 sn = __ldg(reinterpret_cast<const float2*>(t + D / 2 + ch.fbase[p] + 2 * e));
+          rsc[row][p][e] = ptx::f2(c.x, c.y);
+          rss[row][p][e] = ptx::f2(sn.x, sn.y);
         }
       }
     }
@@ -211,7 +233,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < GE::NCH; ++i) qw[nt][i] = scale_chunk(qraw[nt][i], qs);
+      for (int i = 0; i < GE::NCH; ++i) qw[nt][i] = qraw[nt][i];
   }
 
   float mrun[NT][2], lrun[NT][2];
@@ -226,27 +248,37 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
       for (int k = 0; k < 4; ++k) oacc[mt][nt][k] = 0.f;
   }
 
-  const int* bt = a.block_tables + (size_t)r * mb;
-  const int* bs_ = a.block_starts + (size_t)r * mb;
+  __syncthreads();  // meta visible, barriers initialised
 
-  // lane 0: issue the k-th block of this warp into its stage
+  // lane 0: issue the k-th block of this warp into its stage: K and V tiles by
+  // TMA, plus the table row |t - start| the block's query rotation needs
   auto issue = [&](int k) {
-    const int b = b_begin + warp + kWarps * k;
+    const int i = warp + kWarps * k;
     const int stg = k % kStages;
     const uint32_t bar = bar_base + (warp * kStages + stg) * 8;
     const uint32_t kdst = sbase + (warp * kStages + stg) * GE::STAGE;
-    const int phys = __ldg(bt + b);
+    const int phys = meta[2 * i];
     if (phys < 0 || phys >= a.num_blocks) {
       ptx::mbar_arrive(bar);  // nothing to load; the consumer masks the block
       return;
     }
-    ptx::mbar_arrive_expect_tx(bar, 2 * GE::TILE);
+    int ad = 0;
+    bool row_ok = false;
+    if constexpr (ROPE) {
+      const int delta = tq - meta[2 * i + 1];
+      ad = delta < 0 ? -delta : delta;
+      row_ok = ad < a.max_pos;
+    }
+    ptx::mbar_arrive_expect_tx(bar, 2 * GE::TILE + (row_ok ? SM::ROWB : 0));
     const int y = (phys * a.Hkv + hk) * 16;
 #pragma unroll
     for (int hh = 0; hh < GE::HALVES; ++hh) {
       ptx::tma_load_2d(kdst + hh * 2048, &kmap, 64 * hh, y, bar);
       ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
     }
+    if (row_ok)
+      ptx::bulk_load(sbase + SM::ROWS + (warp * kStages + stg) * SM::ROWB, a.cos_sin + (size_t)ad * D, SM::ROWB,
+                     bar);
   };
   if (lane == 0) {
     const int pre = nmine < kStages ? nmine : kStages;
@@ -256,53 +288,31 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
   bool timed_out = false;
   int k_stop = nmine;
   for (int k = 0; k < nmine; ++k) {
-    const int b = b_begin + warp + kWarps * k;
+    const int i = warp + kWarps * k;
+    const int b = b_begin + i;
     const int stg = k % kStages;
     const uint32_t bar = bar_base + (warp * kStages + stg) * 8;
     const uint32_t kbase = sbase + (warp * kStages + stg) * GE::STAGE;
     const uint32_t vbase = kbase + GE::TILE;
+    const uint32_t rowb = sbase + SM::ROWS + (warp * kStages + stg) * SM::ROWB;
 
-    const int phys = __ldg(bt + b);
+    const int phys = meta[2 * i];
     const bool ok = phys >= 0 && phys < a.num_blocks;
-    const int start = ROPE ? __ldg(bs_ + b) : 0;
+    const int start = meta[2 * i + 1];
     const int nk = min(16, L - b * 16);
-    bool v0 = ok && g8 < nk, v1 = ok && g8 + 8 < nk;
+    bool v0 = ok && ks0 < nk, v1 = ok && ks0 + 8 < nk;
     if (!ok && lane == 0) atomicOr(a.err, kErrBlockId);
-
-    // re-rotate q by t - start (overlaps the wait for the tiles)
+    int delta = 0;
     if constexpr (ROPE) {
-      const int delta = tq - start;
+      delta = tq - start;
       const int ad = delta < 0 ? -delta : delta;
-      const bool pos_ok = ad < a.max_pos && start >= 0 && start + nk - 1 < a.max_pos;
-      const int arow = ad < a.max_pos ? ad : 0;
-      if (ok && !pos_ok) {
+      if (ok && !(ad < a.max_pos && start >= 0 && start + nk - 1 < a.max_pos)) {
         // keys whose position falls outside the table are masked
-        const bool p0 = start + g8 >= 0 && start + g8 < a.max_pos && ad < a.max_pos;
-        const bool p1 = start + g8 + 8 >= 0 && start + g8 + 8 < a.max_pos && ad < a.max_pos;
+        const bool p0 = start + ks0 >= 0 && start + ks0 < a.max_pos && ad < a.max_pos;
+        const bool p1 = start + ks0 + 8 >= 0 && start + ks0 + 8 < a.max_pos && ad < a.max_pos;
         if (__any_sync(0xffffffffu, (v0 && !p0) || (v1 && !p1)) && lane == 0) atomicOr(a.err, kErrPosition);
         v0 = v0 && p0;
         v1 = v1 && p1;
-      }
-      const float* trow = a.cos_sin + (size_t)arow * D;
-      const float sg = (delta < 0 ? -ch.sigma : ch.sigma) * qs;
-#pragma unroll
-      for (int p = 0; p < GE::NPAIR; ++p) {
-        float c[8], s[8];
-        const float4 c0 = __ldg(reinterpret_cast<const float4*>(trow + ch.fbase[p]));
-        const float4 c1 = __ldg(reinterpret_cast<const float4*>(trow + ch.fbase[p] + 4));
-        const float4 s0 = __ldg(reinterpret_cast<const float4*>(trow + D / 2 + ch.fbase[p]));
-        const float4 s1 = __ldg(reinterpret_cast<const float4*>(trow + D / 2 + ch.fbase[p] + 4));
-        c[0] = c0.x * qs; c[1] = c0.y * qs; c[2] = c0.z * qs; c[3] = c0.w * qs;
-        c[4] = c1.x * qs; c[5] = c1.y * qs; c[6] = c1.z * qs; c[7] = c1.w * qs;
-        s[0] = s0.x * sg; s[1] = s0.y * sg; s[2] = s0.z * sg; s[3] = s0.w * sg;
-        s[4] = s1.x * sg; s[5] = s1.y * sg; s[6] = s1.z * sg; s[7] = s1.w * sg;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          U4 x = qraw[nt][ch.first[p]], y = qraw[nt][ch.second[p]];
-          rotate_pair(x, y, c, s);
-          qw[nt][ch.first[p]] = x;
-          qw[nt][ch.second[p]] = y;
-        }
       }
     }
 
@@ -315,70 +325,119 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
       break;
     }
 
+    // re-rotate q by t - start from the staged table row
+    if constexpr (ROPE) {
+      const float sg = delta < 0 ? -1.f : 1.f;
+#pragma unroll
+      for (int p = 0; p < GE::NPAIR; ++p) {
+        const U4 c0 = ptx::lds128(rowb + 4 * ch.fbase[p]);
+        const U4 c1 = ptx::lds128(rowb + 4 * ch.fbase[p] + 16);
+        const U4 s0 = ptx::lds128(rowb + 2 * D + 4 * ch.fbase[p]);
+        const U4 s1 = ptx::lds128(rowb + 2 * D + 4 * ch.fbase[p] + 16);
+        uint64_t c2[4], s2[4];
+        c2[0] = ptx::f2(__uint_as_float(c0.x), __uint_as_float(c0.y));
+        c2[1] = ptx::f2(__uint_as_float(c0.z), __uint_as_float(c0.w));
+        c2[2] = ptx::f2(__uint_as_float(c1.x), __uint_as_float(c1.y));
+        c2[3] = ptx::f2(__uint_as_float(c1.z), __uint_as_float(c1.w));
+        s2[0] = ptx::f2(sg * __uint_as_float(s0.x), sg * __uint_as_float(s0.y));
+        s2[1] = ptx::f2(sg * __uint_as_float(s0.z), sg * __uint_as_float(s0.w));
+        s2[2] = ptx::f2(sg * __uint_as_float(s1.x), sg * __uint_as_float(s1.y));
+        s2[3] = ptx::f2(sg * __uint_as_float(s1.z), sg * __uint_as_float(s1.w));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          U4 x = qraw[nt][ch.first[p]], y = qraw[nt][ch.second[p]];
+          rotate_pair(x, y, c2, s2);
+          qw[nt][ch.first[p]] = x;
+          qw[nt][ch.second[p]] = y;
+        }
+      }
+    }
+
     // key rows g8 and g8 + 8 of the block, rotated by R_slot in registers
     U4 kr[2][GE::NCH];
 #pragma unroll
     for (int row = 0; row < 2; ++row)
 #pragma unroll
-      for (int i = 0; i < GE::NCH; ++i) kr[row][i] = ptx::lds128(kbase + swz(ch.h[i], g8 + 8 * row, ch.c[i]));
+      for (int c = 0; c < GE::NCH; ++c) kr[row][c] = ptx::lds128(kbase + swz(ch.h[c], ks0 + 8 * row, ch.c[c]));
     if constexpr (ROPE) {
 #pragma unroll
       for (int row = 0; row < 2; ++row)
 #pragma unroll
-        for (int p = 0; p < GE::NPAIR; ++p) rotate_pair(kr[row][ch.first[p]], kr[row][ch.second[p]], rsc[row][p], rss[row][p]);
+        for (int p = 0; p < GE::NPAIR; ++p)
+          rotate_pair(kr[row][ch.first[p]], kr[row][ch.second[p]], rsc[row][p], rss[row][p]);
     }
 
-    // S^T = K' Q'^T
-    float sacc[NT][4];
+    // S^T = K' Q'^T, two independent accumulation chains (even / odd k-steps)
+    float sacc[NT][4], sacc2[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < GE::NCH; ++i) {
+      for (int e = 0; e < 4; ++e) sacc[nt][e] = sacc2[nt][e] = 0.f;
+#pragma unroll
+    for (int c = 0; c < GE::NCH; ++c) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const uint32_t a0 = w_of(kr[0][i], 2 * u), a1 = w_of(kr[1][i], 2 * u);
-        const uint32_t a2 = w_of(kr[0][i], 2 * u + 1), a3 = w_of(kr[1][i], 2 * u + 1);
+        const uint32_t a0 = w_of(kr[0][c], 2 * u), a1 = w_of(kr[1][c], 2 * u);
+        const uint32_t a2 = w_of(kr[0][c], 2 * u + 1), a3 = w_of(kr[1][c], 2 * u + 1);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          ptx::mma_bf16_16816(sacc[nt], a0, a1, a2, a3, w_of(qw[nt][i], 2 * u), w_of(qw[nt][i], 2 * u + 1));
+        for (int nt = 0; nt < NT; ++nt) {
+          if (u == 0)
+            ptx::mma_bf16_16816(sacc[nt], a0, a1, a2, a3, w_of(qw[nt][c], 0), w_of(qw[nt][c], 1));
+          else
+            ptx::mma_bf16_16816(sacc2[nt], a0, a1, a2, a3, w_of(qw[nt][c], 2), w_of(qw[nt][c], 3));
+        }
       }
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
 
     // online softmax over the 16 keys, per head column (2 tig + j) of each n-tile
     uint32_t pb0[NT], pb1[NT];
+    float corr[NT][2];
+    bool any_corr = false;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float pv[4];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const float sa = v0 ? sacc[nt][j] : -CUDART_INF_F;
-        const float sb = v1 ? sacc[nt][2 + j] : -CUDART_INF_F;
+        const float sa = v0 ? sacc[nt][j] * qs : -CUDART_INF_F;
+        const float sb = v1 ? sacc[nt][2 + j] * qs : -CUDART_INF_F;
         float bm = fmaxf(sa, sb);
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
         const float mnew = fmaxf(mrun[nt][j], bm);
         const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
-        const float corr = exp2f(mrun[nt][j] - muse);
+        corr[nt][j] = exp2f(mrun[nt][j] - muse);
+        any_corr |= mnew != mrun[nt][j];
         const float pa = exp2f(sa - muse), pbv = exp2f(sb - muse);
-        lrun[nt][j] = fmaf(lrun[nt][j], corr, pa + pbv);
+        lrun[nt][j] = fmaf(lrun[nt][j], corr[nt][j], pa + pbv);
         mrun[nt][j] = mnew;
-#pragma unroll
-        for (int mt = 0; mt < GE::MT; ++mt) {
-          oacc[mt][nt][j] *= corr;
-          oacc[mt][nt][2 + j] *= corr;
-        }
         pv[j] = pa;
         pv[2 + j] = pbv;
       }
       pb0[nt] = ptx::movmatrix_trans(ptx::pack_bf16(pv[0], pv[1]));  // keys 0..7
       pb1[nt] = ptx::movmatrix_trans(ptx::pack_bf16(pv[2], pv[3]));  // keys 8..15
     }
+    // rescale the accumulators only when some running max moved
+    if (__any_sync(0xffffffffu, any_corr)) {
+#pragma unroll
+      for (int mt = 0; mt < GE::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            oacc[mt][nt][j] *= corr[nt][j];
+            oacc[mt][nt][2 + j] *= corr[nt][j];
+          }
+    }
 
     // O^T += V^T P^T
     {
       const int mi = lane >> 3, rr = lane & 7;
-      const int key = rr + 8 * (mi >> 1);
+      const int key = frag_slot(rr) + 8 * (mi >> 1);
 #pragma unroll
       for (int mt = 0; mt < GE::MT; ++mt) {
         const int cg = 2 * mt + (mi & 1);
@@ -394,7 +453,6 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
   }
 
   if (timed_out) {
-    // let copies already issued land before the CTA exits (bounded)
     // blocks k_stop .. k_stop + kStages - 1 were issued and not consumed
     if (lane == 0) {
       const int last = min(nmine, k_stop + kStages);
@@ -405,7 +463,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
     }
   }
 
-  // per-warp state -> this warp's own stage region: m[16], l[16], O[16][D]
+  // per-warp state -> this warp's own stage region: m[16], l[16], O[16][D + 4]
+  constexpr int OST = D + 4;  // padded row stride (conflict-free stores)
   float* wm = reinterpret_cast<float*>(sgen + warp * kStages * GE::STAGE);
   float* wl = wm + 16;
   float* wo = wm + 32;
@@ -436,8 +495,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int head = 8 * nt + 2 * tig + j;
-        wo[head * D + 16 * mt + g8] = oacc[mt][nt][j];
-        wo[head * D + 16 * mt + g8 + 8] = oacc[mt][nt][2 + j];
+        wo[head * OST + 16 * mt + g8] = oacc[mt][nt][j];
+        wo[head * OST + 16 * mt + g8 + 8] = oacc[mt][nt][2 + j];
       }
   __syncthreads();
 
@@ -455,7 +514,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
       const float mw = base[head];
       const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
       Ls = fmaf(base[16 + head], f, Ls);
-      O = fmaf(base[32 + head * D + dim], f, O);
+      O = fmaf(base[32 + head * OST + dim], f, O);
     }
     const int hq = hk * G + head;
     if (direct) {
@@ -505,7 +564,7 @@ bool make_pool_map(CUtensorMap* m, const void* base, long long rows, int D) {
 template <int D, int NT, bool ROPE>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
   using GE = Geo<D>;
-  const int smem = kWarps * kStages * GE::STAGE + kWarps * kStages * 8 + 1024;
+  const int smem = Smem<D>::TOTAL + 1024;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
