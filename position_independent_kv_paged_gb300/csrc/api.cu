@@ -254,18 +254,53 @@ size_t minipic_attn_prefill_workspace_size(int32_t, int32_t, int32_t, int32_t, i
 }
 
 minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
-                                    const minipic_rope* rope, const minipic_prefill_batch* batch, float scale,
+                                    const minipic_rope* rope, const minipic_prefill_batch* b, float scale,
                                     void* workspace, size_t workspace_bytes, minipic_stream_t stream) {
-  (void)num_q_heads;
-  (void)kv;
-  (void)rope;
-  (void)batch;
-  (void)scale;
   (void)workspace;
   (void)workspace_bytes;
-  (void)stream;
+  if (dtype != MINIPIC_F32 && dtype != MINIPIC_BF16) return MINIPIC_ERR_INVALID;
+  if (!b) return MINIPIC_ERR_INVALID;
+  minipic_status st = check_pool(kv, num_q_heads, b->batch > 0);
+  if (st != MINIPIC_OK) return st;
+  st = check_rope(rope, kv->head_dim);
+  if (st != MINIPIC_OK) return st;
   if (dtype != MINIPIC_BF16) return MINIPIC_ERR_UNSUPPORTED;
-  return MINIPIC_ERR_UNSUPPORTED;
+  if (b->batch < 0 || b->total_q < 0 || b->max_q_len < 0 || b->max_blocks_per_seq < 0) return MINIPIC_ERR_INVALID;
+  if (b->batch == 0 || b->total_q == 0) return MINIPIC_OK;
+  if (b->max_q_len == 0 || b->max_blocks_per_seq == 0 || kv->num_blocks == 0) return MINIPIC_ERR_INVALID;
+  if (!b->q || !b->cu_q_lens || !b->q_pos || !b->block_tables || !b->block_starts || !b->kv_lens || !b->out)
+    return MINIPIC_ERR_INVALID;
+  if (!aligned16(b->q) || !aligned16(b->out)) return MINIPIC_ERR_INVALID;
+  if (!isfinite(scale)) return MINIPIC_ERR_INVALID;
+  int* err = nullptr;
+  if (device_info(&err, nullptr) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  PrefillArgs a{};
+  a.q = b->q;
+  a.cu_q_lens = b->cu_q_lens;
+  a.q_pos = b->q_pos;
+  a.k_pool = kv->k_pool;
+  a.v_pool = kv->v_pool;
+  a.block_tables = b->block_tables;
+  a.block_starts = b->block_starts;
+  a.kv_lens = b->kv_lens;
+  a.cos_sin = rope->cos_sin;
+  a.max_pos = rope->max_pos;
+  a.out = b->out;
+  a.lse = b->lse;
+  a.batch = b->batch;
+  a.total_q = b->total_q;
+  a.max_q_len = b->max_q_len;
+  a.Hq = num_q_heads;
+  a.Hkv = kv->num_kv_heads;
+  a.G = num_q_heads / kv->num_kv_heads;
+  a.D = kv->head_dim;
+  a.BS = kv->block_size;
+  a.num_blocks = kv->num_blocks;
+  a.max_blocks = b->max_blocks_per_seq;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)kv->head_dim);
+  a.err = err;
+  const cudaError_t e = launch_prefill_tc(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 
 minipic_status minipic_device_error(int32_t* flags_out, int32_t clear, minipic_stream_t stream) {

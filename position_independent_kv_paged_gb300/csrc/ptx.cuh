@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace minipic {
@@ -127,6 +128,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 // ---------------------------------------------------------------- packed fp32 pairs (sm_100+ f32x2)
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
   uint64_t d;
@@ -159,6 +165,12 @@ __device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) {
   float lo, hi;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
   return pack_bf16(lo, hi);
+}
+// fp32 pair -> f16x2 word, round to nearest even
+__device__ __forceinline__ uint32_t f2_to_h2(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return pack_f16(lo, hi);
 }
 
 // L2 eviction policies (createpolicy)

@@ -1,0 +1,96 @@
+"""Chunked-prefill parity: the tcgen05 CUDA path (through the C ABI) against the
+CPU oracle, on RAG-shaped, causal-from-zero and irregular inputs."""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import TOL, compare, compare_lse, upload_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from position_independent_kv_paged_gb300 import _build
+    _build.build()
+    import position_independent_kv_paged_gb300 as mp
+    mp.load()
+    return torch, mp, torch.device("cuda:0")
+
+
+def run_prefill(env, w):
+    torch, mp, dev = env
+    p = w.prefill
+    t = upload_prefill(w, torch, dev)
+    rope = mp.rope_table(w.max_pos, w.d, w.rope_base, device=dev)
+    lse = torch.full((int(p.cu_q_lens[-1]), w.Hq), float("nan"), dtype=torch.float32, device=dev)
+    max_q = int(np.diff(p.cu_q_lens).max()) if p.batch else 1
+    out, _ = mp.attn_prefill(t["q"], t["cu_q_lens"], t["q_pos"], t["k_pool"], t["v_pool"], t["block_tables"],
+                             t["block_starts"], t["kv_lens"], rope, max_q_len=max_q, lse=lse)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def test_rag_prefill_scaled(env):
+    w = W.rag_prefill(1, B=3, n_spans=2, span_tokens=256, pool_spans=6, q_len=200)
+    out, lse = run_prefill(env, w)
+    ref, rl = oracle.prefill(w)
+    compare(out, ref, "bf16", "rag_prefill small")
+    compare_lse(lse, rl, "bf16", "rag_prefill small")
+    assert env[1].device_error() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(28, 4), (8, 8), (16, 1), (32, 8)])
+def test_causal_span_prefill_from_zero(env, Hq, Hkv):
+    w = W.mixed_batch(2, n_prefill=3, chunk=300, n_decode=0, Hq=Hq, Hkv=Hkv)
+    out, lse = run_prefill(env, w)
+    ref, rl = oracle.prefill(w)
+    compare(out, ref, "bf16", f"span prefill {Hq}/{Hkv}")
+    compare_lse(lse, rl, "bf16", "span prefill")
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (12, 4, 64), (7, 1, 128), (4, 4, 64)])
+def test_irregular_prefill(env, Hq, Hkv, d):
+    w = W.irregular_prefill(5 + Hq, "bf16", kv_lens=[1, 17, 300, 129, 513], q_lens=[1, 5, 300, 1, 77], Hq=Hq,
+                            Hkv=Hkv, d=d, max_pos=60000)
+    out, lse = run_prefill(env, w)
+    ref, rl = oracle.prefill(w)
+    compare(out, ref, "bf16", f"irregular prefill {Hq}/{Hkv}/{d}")
+    compare_lse(lse, rl, "bf16", "irregular prefill")
+
+
+def test_prefill_rejects_f32(env):
+    torch, mp, dev = env
+    w = W.irregular_prefill(3, "f32", kv_lens=[20], q_lens=[4], Hq=4, Hkv=2, d=128, max_pos=100)
+    with pytest.raises(mp.MiniPICError) as e:
+        run_prefill(env, w)
+    assert e.value.status == 2
+
+
+def test_prefill_flags_bad_block_ids(env):
+    torch, mp, dev = env
+    w = W.irregular_prefill(8, "bf16", kv_lens=[100, 60], q_lens=[30, 60], Hq=4, Hkv=2, d=128, max_pos=1000)
+    mp.device_error(clear=True)
+    w.prefill.block_tables[1, 2] = 10 ** 6
+    out, _ = run_prefill(env, w)
+    assert mp.device_error(clear=True) & 1
+    assert np.all(np.isfinite(out))
+
+
+@pytest.mark.parametrize("idx,sample", [(2, [0, 5]), (4, [3, 12])])
+def test_full_size_prefill_sampled(env, idx, sample):
+    w = W.config(idx)
+    if idx == 4:
+        w.decode = None
+    out, lse = run_prefill(env, w)
+    ref, rl = oracle.prefill(w, requests=sample)
+    rows = np.concatenate([np.arange(w.prefill.cu_q_lens[r], w.prefill.cu_q_lens[r + 1]) for r in sample])
+    compare(out[rows], ref[rows], "bf16", f"config {idx} sampled")
+    compare_lse(lse[rows], rl[rows], "bf16", f"config {idx} sampled")
+    assert np.all(np.isfinite(out))
+    assert env[1].device_error() == 0
