@@ -229,6 +229,48 @@ class DecodeCase:
         return 2 if self.ws_n > 0 else 1
 
 
+def prefill_flops(w) -> int:
+    """Algorithmic FLOPs of one prefill call: QK^T and PV over the allowed
+    (causal) keys only: 4 * Hq * d * sum_rows (kv_len - q_len + i + 1)."""
+    p = w.prefill
+    tot = 0
+    for r in range(p.batch):
+        ql = int(p.cu_q_lens[r + 1] - p.cu_q_lens[r])
+        kv = int(p.kv_lens[r])
+        tot += ql * (kv - ql) + ql * (ql + 1) // 2
+    return 4 * w.Hq * w.d * tot
+
+
+class PrefillCase:
+    """A prefill workload resident on the GPU, timed through the C ABI."""
+
+    def __init__(self, w, dev, torch, mp):
+        import numpy as np
+        self.w, self.torch, self.mp = w, torch, mp
+        p = w.prefill
+
+        def up(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.kpool, self.vpool, self.q = up(w.kv.k_pool), up(w.kv.v_pool), up(p.q)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+        self.cu, self.qp, self.kvl = i32(p.cu_q_lens), i32(p.q_pos), i32(p.kv_lens)
+        self.bt, self.st = i32(p.block_tables), i32(p.block_starts)
+        self.max_q = int(np.diff(p.cu_q_lens).max())
+        self.rope = mp.rope_table(w.max_pos, w.d, w.rope_base, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[0], w.Hq, dtype=torch.float32, device=dev)
+        self.flops = prefill_flops(w)
+
+    def step(self):
+        self.mp.attn_prefill(self.q, self.cu, self.qp, self.kpool, self.vpool, self.bt, self.st, self.kvl,
+                             self.rope, max_q_len=self.max_q, out=self.out, lse=self.lse)
+
+    def step_norope(self):
+        self.mp.attn_prefill_prerotated(self.q, self.cu, self.qp, self.kpool, self.vpool, self.bt, self.st,
+                                        self.kvl, max_q_len=self.max_q, out=self.out, lse=self.lse)
+
+
 def timed(torch, stream, flush, fn, steps):
     """Per-step CUDA-event times (ms); L2 flushed before every step, outside the events."""
     evs = []
@@ -366,6 +408,26 @@ def run_minipic(args):
                 raise RuntimeError(f"device error in {name}")
             del cx, wx
             torch.cuda.empty_cache()
+
+        # chunked prefill over cached spans: TFLOP/s against the bf16 tensor peak
+        wp = W.rag_prefill(seed=rank)
+        cp = PrefillCase(wp, dev, torch, mp)
+        for _ in range(3):
+            cp.step()
+        mp_ = timed(torch, stream, flush, cp.step, args.steps)
+        mp_ = sum(mp_) / len(mp_)
+        for _ in range(3):
+            cp.step_norope()
+        mpn = timed(torch, stream, flush, cp.step_norope, args.steps)
+        mpn = sum(mpn) / len(mpn)
+        tf = cp.flops / (mp_ * 1e-3) / 1e12
+        extras["prefill"] = {"workload": f"{wp.name}: {wp.notes}", "ms_per_step": mp_, "TFLOP_s": tf,
+                             "frac_of_bf16_peak": tf / pk["bf16"], "peak_TFLOP_s": pk["bf16"],
+                             "algorithmic_flops": cp.flops, "rope_off_ms": mpn, "rope_overhead": mp_ / mpn - 1.0}
+        if mp.device_error() != 0:
+            raise RuntimeError("device error in prefill")
+        del cp, wp
+        torch.cuda.empty_cache()
 
     if rank == 0:
         line = {

@@ -208,13 +208,24 @@ size_t minipic_attn_prefill_workspace_size(int32_t batch, int32_t num_q_heads, i
 /* Chunked prefill over cached span blocks plus the chunk's own keys (the
  * uncached-span prefill of MiniPIC section 4 and the final-prompt prefill that
  * reads cached spans).  Keys are rotated at pi(j) into shared memory and the
- * products run on the tcgen05 tensor cores with TMEM accumulators.  bf16 only
- * (f32 returns UNSUPPORTED).  Errors as for decode. */
+ * products run on the tcgen05 tensor cores with TMEM accumulators.  The
+ * rotated q and k are rounded to fp16 for the QK^T product (10-bit mantissa:
+ * rotated elements must stay within +-65504); softmax weights and V are bf16
+ * for the P.V product; accumulation is fp32.  bf16 only (f32 returns
+ * UNSUPPORTED).  The workspace is not used (size 0).  Errors as for decode. */
 minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads,
                                     const minipic_kv_pool* kv, const minipic_rope* rope,
                                     const minipic_prefill_batch* batch, float scale,
                                     void* workspace, size_t workspace_bytes,
                                     minipic_stream_t stream);
+
+/* The same prefill kernel with the rotation compiled out: keys in the pool and
+ * q are taken as already rotated (standard paged prefill over a pre-rotated
+ * cache, bf16 products).  It exists to measure what on-the-fly rotation costs;
+ * no table is needed.  bf16 only.  Errors as for minipic_attn_prefill. */
+minipic_status minipic_attn_prefill_prerotated(minipic_dtype dtype, int32_t num_q_heads,
+                                               const minipic_kv_pool* kv, const minipic_prefill_batch* batch,
+                                               float scale, minipic_stream_t stream);
 
 /* Read the device error word (MINIPIC_DEVERR_* bits, 0 if none) of the current
  * device after the work queued on `stream` has finished (this call

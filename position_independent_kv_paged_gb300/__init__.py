@@ -31,6 +31,7 @@ __all__ = [
     "attn_decode_prerotated",
     "prefill_workspace_size",
     "attn_prefill",
+    "attn_prefill_prerotated",
     "device_error",
     "STATUS",
 ]
@@ -112,6 +113,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         L.minipic_attn_prefill.restype = ctypes.c_int
         L.minipic_attn_prefill.argtypes = [ctypes.c_int, c_i32, ctypes.POINTER(_KV), ctypes.POINTER(_Rope),
                                            ctypes.POINTER(_Prefill), c_f, c_vp, c_sz, c_vp]
+        L.minipic_attn_prefill_prerotated.restype = ctypes.c_int
+        L.minipic_attn_prefill_prerotated.argtypes = [ctypes.c_int, c_i32, ctypes.POINTER(_KV),
+                                                      ctypes.POINTER(_Prefill), c_f, c_vp]
         L.minipic_device_error.restype = ctypes.c_int
         L.minipic_device_error.argtypes = [ctypes.POINTER(c_i32), c_i32, c_vp]
         _lib = L
@@ -254,9 +258,8 @@ def prefill_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_q_len
                                                           max_q_len, max_blocks_per_seq, block_size))
 
 
-def attn_prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv_lens, rope,
-                 max_q_len: int, scale: float = 0.0, out=None, lse=None, workspace=None, stream=None):
-    """Chunked prefill (bf16) over cached span blocks plus the chunk's own keys."""
+def _prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv_lens, rope, max_q_len, scale,
+             out, lse, workspace, stream, prerotated):
     torch = _torch()
     L = load()
     _need(q, "q", ndim=3)
@@ -266,25 +269,44 @@ def attn_prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts
         _need(t, name, dtype=torch.int32, ndim=2)
     for name, t in (("cu_q_lens", cu_q_lens), ("q_pos", q_pos), ("kv_lens", kv_lens)):
         _need(t, name, dtype=torch.int32, ndim=1)
-    _need(rope, "rope", dtype=torch.float32, ndim=2)
     if out is None:
         out = torch.empty_like(q)
     if lse is not None:
         _need(lse, "lse", dtype=torch.float32)
     B = kv_lens.shape[0]
     mb = block_tables.shape[1]
-    if workspace is None:
-        n = prefill_workspace_size(B, Hq, kv.num_kv_heads, d, max_q_len, mb, kv.block_size)
-        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
     pb = _Prefill(q.data_ptr(), cu_q_lens.data_ptr(), q_pos.data_ptr(), block_tables.data_ptr(),
                   block_starts.data_ptr(), kv_lens.data_ptr(), B, total_q, int(max_q_len), mb,
                   out.data_ptr(), _ptr(lse))
+    if prerotated:
+        st = L.minipic_attn_prefill_prerotated(_dtype_code(q), Hq, ctypes.byref(kv), ctypes.byref(pb),
+                                               float(scale), _stream(stream))
+        _check(st, "minipic_attn_prefill_prerotated")
+        return out, lse
+    _need(rope, "rope", dtype=torch.float32, ndim=2)
+    if workspace is None:
+        n = prefill_workspace_size(B, Hq, kv.num_kv_heads, d, max_q_len, mb, kv.block_size)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
     rp = _Rope(rope.data_ptr(), rope.shape[0], rope.shape[1])
     st = L.minipic_attn_prefill(_dtype_code(q), Hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(pb),
                                 float(scale), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "minipic_attn_prefill")
     return out, lse
+
+
+def attn_prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv_lens, rope,
+                 max_q_len: int, scale: float = 0.0, out=None, lse=None, workspace=None, stream=None):
+    """Chunked prefill (bf16) over cached span blocks plus the chunk's own keys."""
+    return _prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv_lens, rope, max_q_len,
+                    scale, out, lse, workspace, stream, False)
+
+
+def attn_prefill_prerotated(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv_lens,
+                            max_q_len: int, scale: float = 0.0, out=None, lse=None, stream=None):
+    """Same prefill kernel with rotation compiled out (keys and q already rotated)."""
+    return _prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv_lens, None, max_q_len,
+                    scale, out, lse, None, stream, True)
 
 
 def device_error(clear: bool = True, stream=None) -> int:

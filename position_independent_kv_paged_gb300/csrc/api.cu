@@ -253,17 +253,21 @@ size_t minipic_attn_prefill_workspace_size(int32_t, int32_t, int32_t, int32_t, i
   return 0;
 }
 
-minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
-                                    const minipic_rope* rope, const minipic_prefill_batch* b, float scale,
-                                    void* workspace, size_t workspace_bytes, minipic_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
+}  // extern "C"
+
+namespace {
+
+minipic_status prefill_common(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                              const minipic_rope* rope, const minipic_prefill_batch* b, float scale,
+                              cudaStream_t stream, bool rotate) {
   if (dtype != MINIPIC_F32 && dtype != MINIPIC_BF16) return MINIPIC_ERR_INVALID;
   if (!b) return MINIPIC_ERR_INVALID;
   minipic_status st = check_pool(kv, num_q_heads, b->batch > 0);
   if (st != MINIPIC_OK) return st;
-  st = check_rope(rope, kv->head_dim);
-  if (st != MINIPIC_OK) return st;
+  if (rotate) {
+    st = check_rope(rope, kv->head_dim);
+    if (st != MINIPIC_OK) return st;
+  }
   if (dtype != MINIPIC_BF16) return MINIPIC_ERR_UNSUPPORTED;
   if (b->batch < 0 || b->total_q < 0 || b->max_q_len < 0 || b->max_blocks_per_seq < 0) return MINIPIC_ERR_INVALID;
   if (b->batch == 0 || b->total_q == 0) return MINIPIC_OK;
@@ -283,8 +287,8 @@ minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads, co
   a.block_tables = b->block_tables;
   a.block_starts = b->block_starts;
   a.kv_lens = b->kv_lens;
-  a.cos_sin = rope->cos_sin;
-  a.max_pos = rope->max_pos;
+  a.cos_sin = rotate ? rope->cos_sin : nullptr;
+  a.max_pos = rotate ? rope->max_pos : 0;
   a.out = b->out;
   a.lse = b->lse;
   a.batch = b->batch;
@@ -299,8 +303,26 @@ minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads, co
   a.max_blocks = b->max_blocks_per_seq;
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)kv->head_dim);
   a.err = err;
-  const cudaError_t e = launch_prefill_tc(a, (cudaStream_t)stream);
+  const cudaError_t e = launch_prefill_tc(a, rotate, stream);
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                                    const minipic_rope* rope, const minipic_prefill_batch* batch, float scale,
+                                    void* workspace, size_t workspace_bytes, minipic_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  return prefill_common(dtype, num_q_heads, kv, rope, batch, scale, (cudaStream_t)stream, true);
+}
+
+minipic_status minipic_attn_prefill_prerotated(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                                               const minipic_prefill_batch* batch, float scale,
+                                               minipic_stream_t stream) {
+  return prefill_common(dtype, num_q_heads, kv, nullptr, batch, scale, (cudaStream_t)stream, false);
 }
 
 minipic_status minipic_device_error(int32_t* flags_out, int32_t clear, minipic_stream_t stream) {

@@ -65,6 +65,6 @@ cudaError_t launch_decode(const DecodeArgs& a, bool bf16, bool rotate, const Dec
 cudaError_t launch_decode_simt(const DecodeArgs& a, bool bf16, bool rotate, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool rotate, cudaStream_t s);
 cudaError_t launch_decode_merge(const DecodeArgs& a, bool bf16, cudaStream_t s);
-cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, bool rotate, cudaStream_t s);
 
 }  // namespace minipic

@@ -81,7 +81,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int D>
+template <int D, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const PrefillLaunch L) {
@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* sg = smem_raw + (sbase - ptx::smem_addr(smem_raw));
   int* meta_start = reinterpret_cast<int*>(sg + G_::OFF_META);
   int* meta_flag = meta_start + 8;
-  int* meta_phys = meta_start + 16;
   uint32_t* meta_mask = reinterpret_cast<uint32_t*>(meta_start + 24);  // [2][4]
   const uint32_t bar0 = sbase + G_::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -153,64 +152,72 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       const int* bt = a.block_tables + (size_t)r * mb;
       const int* bs = a.block_starts + (size_t)r * mb;
+      // block ids / starts of the next tile to issue, loaded one tile ahead so that
+      // their global-memory latency overlaps the MMA waits
+      int nph[8], nst[8];
+      int vph[8];  // block ids of the tile whose V is issued next
+      auto load_meta = [&](int t) {
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk) {
+          const int b = 8 * t + blk;
+          nph[blk] = b < nblk ? __ldg(bt + b) : -1;
+          nst[blk] = b < nblk ? __ldg(bs + b) : 0;
+        }
+      };
       auto issue_k = [&](int t) {
         // every compute thread has finished tile t - 2 (it arrived on the rotation
         // barrier of tile t - 1 before this issue), so this parity's words are free
 #pragma unroll
         for (int w = 0; w < 4; ++w) meta_mask[(t & 1) * 4 + w] = 0u;
         int nvalid = 0, nrows = 0;
+#pragma unroll
         for (int blk = 0; blk < 8; ++blk) {
           const int b = 8 * t + blk;
-          int phys = -1, start = 0, flag = 0;
+          int flag = 0;
           if (b < nblk) {
-            phys = __ldg(bt + b);
-            start = __ldg(bs + b);
-            if (phys >= 0 && phys < a.num_blocks) flag |= 1;
+            if (nph[blk] >= 0 && nph[blk] < a.num_blocks) flag |= 1;
             else atomicOr(a.err, kErrBlockId);
-            if (start >= 0 && start < a.max_pos) flag |= 2;
+            if (!ROPE || (nst[blk] >= 0 && nst[blk] < a.max_pos)) flag |= 2;
           }
-          meta_start[blk] = start;
+          meta_start[blk] = nst[blk];
           meta_flag[blk] = flag;
-          meta_phys[blk] = (flag & 1) ? phys : -1;
+          vph[blk] = (flag & 1) ? nph[blk] : -1;
           nvalid += flag & 1;
-          nrows += (flag & 3) == 3;
+          nrows += (ROPE && (flag & 3) == 3) ? 1 : 0;
         }
         ptx::mbar_arrive_expect_tx(bar(kBarKFull), nvalid * G_::HALVES * 2048 + nrows * G_::ROWB);
+#pragma unroll
         for (int blk = 0; blk < 8; ++blk) {
-          if (!(meta_flag[blk] & 1)) continue;
-          const int y = (meta_phys[blk] * a.Hkv + hk) * 16;
+          if (vph[blk] < 0) continue;
+          const int y = (vph[blk] * a.Hkv + hk) * 16;
           for (int hh = 0; hh < G_::HALVES; ++hh)
             ptx::tma_load_2d(sbase + G_::OFF_K + hh * (BN * 128) + blk * 2048, &kmap, 64 * hh, y, bar(kBarKFull));
-          if ((meta_flag[blk] & 3) == 3)
-            ptx::bulk_load(sbase + G_::OFF_RS + blk * G_::ROWB, a.cos_sin + (size_t)meta_start[blk] * D, G_::ROWB,
+          if (ROPE && (meta_flag[blk] & 3) == 3)
+            ptx::bulk_load(sbase + G_::OFF_RS + blk * G_::ROWB, a.cos_sin + (size_t)nst[blk] * D, G_::ROWB,
                            bar(kBarKFull));
         }
       };
-      auto issue_v = [&](int t) {
+      auto issue_v = [&]() {
         int nvalid = 0;
-        int ph[8];
-        for (int blk = 0; blk < 8; ++blk) {
-          const int b = 8 * t + blk;
-          ph[blk] = -1;
-          if (b < nblk) {
-            const int p = __ldg(bt + b);
-            if (p >= 0 && p < a.num_blocks) ph[blk] = p;
-          }
-          nvalid += ph[blk] >= 0;
-        }
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk) nvalid += vph[blk] >= 0 ? 1 : 0;
         ptx::mbar_arrive_expect_tx(bar(kBarVFull), nvalid * G_::HALVES * 2048);
+#pragma unroll
         for (int blk = 0; blk < 8; ++blk) {
-          if (ph[blk] < 0) continue;
-          const int y = (ph[blk] * a.Hkv + hk) * 16;
+          if (vph[blk] < 0) continue;
+          const int y = (vph[blk] * a.Hkv + hk) * 16;
           for (int hh = 0; hh < G_::HALVES; ++hh)
             ptx::tma_load_2d(sbase + G_::OFF_V + hh * (BN * 128) + blk * 2048, &vmap, 64 * hh, y, bar(kBarVFull));
         }
       };
       if (n_kt > 0) {
+        load_meta(0);
         issue_k(0);
-        issue_v(0);
+        issue_v();
+        if (n_kt > 1) load_meta(1);
       }
-      const uint32_t id_qk = umma::idesc_f16_f32(128, BN, false, false);
+      // rotated operands are f16 (10-bit mantissa); the rotation-free variant feeds bf16 as stored
+      const uint32_t id_qk = ROPE ? umma::idesc_f16_f32(128, BN, false, false) : umma::idesc_bf16_f32(128, BN, false, false);
       const uint32_t id_pv = umma::idesc_bf16_f32(128, D, false, true);
       if (!ptx::mbar_wait(bar(kBarQ), 0)) failed = true;
       for (int t = 0; t < n_kt && !failed; ++t) {
@@ -225,7 +232,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         umma::commit(bar(kBarS));
         if (!ptx::mbar_wait(bar(kBarS), par)) { failed = true; break; }
-        if (t + 1 < n_kt) issue_k(t + 1);
+        if (t + 1 < n_kt) {
+          issue_k(t + 1);  // also records the tile's block ids for its V issue
+          if (t + 2 < n_kt) load_meta(t + 2);
+        }
         if (!ptx::mbar_wait(bar(kBarP), par)) { failed = true; break; }
         if (!ptx::mbar_wait(bar(kBarVFull), par)) { failed = true; break; }
         umma::fence_after_sync();
@@ -236,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         umma::commit(bar(kBarPV));
         if (!ptx::mbar_wait(bar(kBarPV), par)) { failed = true; break; }
-        if (t + 1 < n_kt) issue_v(t + 1);
+        if (t + 1 < n_kt) issue_v();
       }
       if (failed) atomicOr(a.err, kErrTimeout);
     }
@@ -257,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                                 ((size_t)(q0 + tq) * a.Hq + (size_t)hk * G + rh) * D;
       int pos = 0;
       if (row_ok) {
-        pos = a.q_pos[q0 + tq];
-        if (pos < 0 || pos >= a.max_pos) {
+        pos = ROPE ? a.q_pos[q0 + tq] : 0;
+        if (ROPE && (pos < 0 || pos >= a.max_pos)) {
           atomicOr(a.err, kErrPosition);
           pos = 0;
         }
@@ -271,9 +281,19 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) qc[c] = U4{0u, 0u, 0u, 0u};
       }
-      const float* trow = a.cos_sin + (size_t)pos * D;
+      if constexpr (!ROPE) {
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {  // chunk c pairs with chunk c + D/16
+        for (int c = 0; c < D / 8; ++c) {
+          U4& x = qc[c];
+          x = U4{ptx::pack_bf16(ptx::bf_lo(x.x) * qs, ptx::bf_hi(x.x) * qs),
+                 ptx::pack_bf16(ptx::bf_lo(x.y) * qs, ptx::bf_hi(x.y) * qs),
+                 ptx::pack_bf16(ptx::bf_lo(x.z) * qs, ptx::bf_hi(x.z) * qs),
+                 ptx::pack_bf16(ptx::bf_lo(x.w) * qs, ptx::bf_hi(x.w) * qs)};
+        }
+      }
+      const float* trow = ROPE ? a.cos_sin + (size_t)pos * D : nullptr;
+#pragma unroll
+      for (int c = 0; c < (ROPE ? D / 16 : 0); ++c) {  // chunk c pairs with chunk c + D/16
         uint64_t c2[4], s2[4];
         const float4 ca = __ldg(reinterpret_cast<const float4*>(trow + 8 * c));
         const float4 cb = __ldg(reinterpret_cast<const float4*>(trow + 8 * c + 4));
@@ -313,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // slot rotation constants cos/sin(s theta_f), f = 8 fg .. 8 fg + 7, for this thread's slots
     uint64_t rsc[G_::SPT][4], rss[G_::SPT][4];
 #pragma unroll
-    for (int u = 0; u < G_::SPT; ++u) {
+    for (int u = 0; u < (ROPE ? G_::SPT : 0); ++u) {
       const int slot = sgp * G_::SPT + u;
       const float* t = a.cos_sin + (size_t)min(slot, a.max_pos - 1) * D;
 #pragma unroll
@@ -342,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int flag = meta_flag[blk];
         const int start = meta_start[blk];
         uint64_t ac[4], as[4];  // cos/sin(start theta_f)
-        if (flag & 2) {
+        if (ROPE && (flag & 2)) {
           const uint32_t rb = sbase + G_::OFF_RS + blk * G_::ROWB;
           const U4 c0 = ptx::lds128(rb + 32 * fg), c1 = ptx::lds128(rb + 32 * fg + 16);
           const U4 s0 = ptx::lds128(rb + 2 * D + 32 * fg), s1 = ptx::lds128(rb + 2 * D + 32 * fg + 16);
@@ -356,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int slot = sgp * G_::SPT + u;
           const int key = blk * 16 + slot;
           const int pos = start + slot;
-          const bool v = (flag & 3) == 3 && 8 * t * 16 + key < kvl && pos < a.max_pos;
+          const bool v = (flag & 3) == 3 && 8 * t * 16 + key < kvl && (!ROPE || pos < a.max_pos);
           kvalid[bb][u] = v;
-          if (!v) continue;
+          if (!ROPE || !v) continue;
           // cos/sin((start + slot) theta) by angle addition
           uint64_t c2[4], s2[4];
 #pragma unroll
@@ -546,7 +566,7 @@ bool make_pool_map(CUtensorMap* m, const void* base, long long rows, int D) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool ROPE>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   const int smem = PG<D>::TOTAL + 1024;
   static bool attr_set[64] = {false};
@@ -554,7 +574,7 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(prefill_tc_kernel<D, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -564,14 +584,15 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   PrefillLaunch L{a, 128 / a.G};
   const int n_qt = (a.max_q_len + L.tq - 1) / L.tq;
   dim3 grid(n_qt, a.Hkv, a.batch);
-  prefill_tc_kernel<D><<<grid, kThreads, smem, s>>>(km, vm, L);
+  prefill_tc_kernel<D, ROPE><<<grid, kThreads, smem, s>>>(km, vm, L);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
-  return a.D == 128 ? launch_t<128>(a, s) : launch_t<64>(a, s);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, bool rotate, cudaStream_t s) {
+  if (rotate) return a.D == 128 ? launch_t<128, true>(a, s) : launch_t<64, true>(a, s);
+  return a.D == 128 ? launch_t<128, false>(a, s) : launch_t<64, false>(a, s);
 }
 
 }  // namespace minipic

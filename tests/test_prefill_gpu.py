@@ -94,3 +94,30 @@ def test_full_size_prefill_sampled(env, idx, sample):
     compare_lse(lse[rows], rl[rows], "bf16", f"config {idx} sampled")
     assert np.all(np.isfinite(out))
     assert env[1].device_error() == 0
+
+
+def test_prerotated_prefill_equals_oracle_on_private_copies(env):
+    """The rotation-free prefill over a cache pre-rotated on the host (every
+    block used by one request) equals the oracle over the unrotated cache."""
+    torch, mp, dev = env
+    # private blocks only (each pre-rotated once); rows attend 401..600 keys
+    w = W.build_workload("private_prefill", 9, "bf16", Hq=8, Hkv=2, d=128, rope_base=500000.0, pool_spans=0,
+                         span_tokens=16, prefill_requests=[([("own", 600)], 200)] * 3)
+    ref, rl = oracle.prefill(w)
+    p = w.prefill
+    k = oracle.widen(w.kv.k_pool, "bf16").copy()
+    q = oracle.widen(p.q, "bf16").copy()
+    for r in range(p.batch):
+        phys, slot, pos = oracle.key_index_map(p.block_tables[r], p.block_starts[r], int(p.kv_lens[r]), 16)
+        for g in range(w.Hkv):
+            k[phys, g, slot] = oracle.rope_rotate(k[phys, g, slot], pos, w.rope_base)
+        q0, q1 = int(p.cu_q_lens[r]), int(p.cu_q_lens[r + 1])
+        for h in range(w.Hq):
+            q[q0:q1, h] = oracle.rope_rotate(q[q0:q1, h], p.q_pos[q0:q1], w.rope_base)
+    w.kv.k_pool = W.to_bf16_bits(k.astype(np.float32))
+    p.q = W.to_bf16_bits(q.astype(np.float32))
+    t = upload_prefill(w, torch, dev)
+    out, _ = mp.attn_prefill_prerotated(t["q"], t["cu_q_lens"], t["q_pos"], t["k_pool"], t["v_pool"],
+                                        t["block_tables"], t["block_starts"], t["kv_lens"], max_q_len=200)
+    torch.cuda.synchronize()
+    compare(out.float().cpu().numpy(), ref, "bf16", "prerotated prefill")
