@@ -213,7 +213,7 @@ class DecodeCase:
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty(d.batch, w.Hq, dtype=torch.float32, device=dev)
         self.ws_n = mp.decode_workspace_size(d.batch, w.Hq, w.Hkv, w.d, self.bt.shape[1])
-        self.ws = torch.empty(max(self.ws_n, 1), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(max(self.ws_n, 1), dtype=torch.uint8, device=dev)
         self.nbytes = decode_kv_bytes(w)
 
     def step(self):

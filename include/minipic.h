@@ -43,7 +43,10 @@
  * -----------------------
  *  The caller owns every buffer.  The library allocates no device memory; entry
  *  points that need scratch take a caller-provided workspace whose size is given
- *  by the matching *_workspace_size query.  All calls are asynchronous on the
+ *  by the matching *_workspace_size query.  The decode workspace starts with
+ *  one completion counter per (request, kv head): zero the workspace once after
+ *  allocating it; every call leaves those counters zero again (after a call that
+ *  reports MINIPIC_DEVERR_TIMEOUT, zero it again before reuse).  All calls are asynchronous on the
  *  given stream (cudaStream_t; NULL = legacy default stream) and act on the
  *  device current at the call.  Inputs must stay valid until the work completes.
  *
@@ -167,6 +170,18 @@ minipic_status minipic_attn_decode(minipic_dtype dtype, int32_t num_q_heads,
                                    const minipic_decode_batch* batch, float scale,
                                    void* workspace, size_t workspace_bytes,
                                    minipic_stream_t stream);
+
+/* Mixed continuous batch in ONE launch: span-prefill chunks (as for
+ * minipic_attn_prefill) and decode tokens (as for minipic_attn_decode) over the
+ * same pool and table, scheduled in one grid so that tensor-core-bound prefill
+ * tiles and HBM-bound decode splits share the SMs (the device side of MiniPIC's
+ * interleaved span-prefill scheduling, section 2.2 "Scheduling").  Either batch
+ * may be empty (batch 0).  Workspace: as for the decode batch
+ * (minipic_attn_decode_workspace_size).  bf16 only.  Errors as above. */
+minipic_status minipic_attn_mixed(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                                  const minipic_rope* rope, const minipic_prefill_batch* prefill,
+                                  const minipic_decode_batch* decode, float scale, void* workspace,
+                                  size_t workspace_bytes, minipic_stream_t stream);
 
 /* The same decode kernel with the rotation compiled out: keys in the pool and
  * q are taken as already rotated (standard paged attention over a pre-rotated

@@ -32,6 +32,7 @@ __all__ = [
     "prefill_workspace_size",
     "attn_prefill",
     "attn_prefill_prerotated",
+    "attn_mixed",
     "device_error",
     "STATUS",
 ]
@@ -116,6 +117,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         L.minipic_attn_prefill_prerotated.restype = ctypes.c_int
         L.minipic_attn_prefill_prerotated.argtypes = [ctypes.c_int, c_i32, ctypes.POINTER(_KV),
                                                       ctypes.POINTER(_Prefill), c_f, c_vp]
+        L.minipic_attn_mixed.restype = ctypes.c_int
+        L.minipic_attn_mixed.argtypes = [ctypes.c_int, c_i32, ctypes.POINTER(_KV), ctypes.POINTER(_Rope),
+                                         ctypes.POINTER(_Prefill), ctypes.POINTER(_Decode), c_f, c_vp, c_sz, c_vp]
         L.minipic_device_error.restype = ctypes.c_int
         L.minipic_device_error.argtypes = [ctypes.POINTER(c_i32), c_i32, c_vp]
         _lib = L
@@ -218,7 +222,7 @@ def _decode(q, k_pool, v_pool, block_tables, block_starts, seq_lens, q_pos, rope
     mb = block_tables.shape[1]
     if workspace is None:
         n = decode_workspace_size(B, Hq, kv.num_kv_heads, d, mb, kv.block_size)
-        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=q.device)
     db = _Decode(q.data_ptr(), block_tables.data_ptr(), block_starts.data_ptr(), seq_lens.data_ptr(),
                  q_pos.data_ptr(), B, mb, out.data_ptr(), _ptr(lse))
     ws_ptr, ws_n = workspace.data_ptr(), workspace.numel() * workspace.element_size()
@@ -307,6 +311,51 @@ def attn_prefill_prerotated(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, b
     """Same prefill kernel with rotation compiled out (keys and q already rotated)."""
     return _prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv_lens, None, max_q_len,
                     scale, out, lse, None, stream, True)
+
+
+def attn_mixed(prefill: dict, decode: dict, k_pool, v_pool, rope, scale: float = 0.0, workspace=None,
+               stream=None):
+    """Span-prefill chunks and decode tokens over one pool in ONE launch.
+
+    ``prefill``: dict with q, cu_q_lens, q_pos, block_tables, block_starts,
+    kv_lens, max_q_len and optional out / lse.  ``decode``: dict with q,
+    block_tables, block_starts, seq_lens, q_pos and optional out / lse.
+    Returns (prefill_out, prefill_lse, decode_out, decode_lse)."""
+    torch = _torch()
+    L = load()
+    kv = _kv(k_pool, v_pool)
+    _need(rope, "rope", dtype=torch.float32, ndim=2)
+    pq, dq = prefill["q"], decode["q"]
+    _need(pq, "prefill q", dtype=k_pool.dtype, ndim=3)
+    _need(dq, "decode q", dtype=k_pool.dtype, ndim=3)
+    for nm in ("cu_q_lens", "q_pos", "kv_lens"):
+        _need(prefill[nm], "prefill " + nm, dtype=torch.int32, ndim=1)
+    for nm in ("block_tables", "block_starts"):
+        _need(prefill[nm], "prefill " + nm, dtype=torch.int32, ndim=2)
+        _need(decode[nm], "decode " + nm, dtype=torch.int32, ndim=2)
+    for nm in ("seq_lens", "q_pos"):
+        _need(decode[nm], "decode " + nm, dtype=torch.int32, ndim=1)
+    pout = prefill.get("out") if prefill.get("out") is not None else torch.empty_like(pq)
+    dout = decode.get("out") if decode.get("out") is not None else torch.empty_like(dq)
+    plse, dlse = prefill.get("lse"), decode.get("lse")
+    Hq = pq.shape[1]
+    pb = _Prefill(pq.data_ptr(), prefill["cu_q_lens"].data_ptr(), prefill["q_pos"].data_ptr(),
+                  prefill["block_tables"].data_ptr(), prefill["block_starts"].data_ptr(),
+                  prefill["kv_lens"].data_ptr(), prefill["kv_lens"].shape[0], pq.shape[0],
+                  int(prefill["max_q_len"]), prefill["block_tables"].shape[1], pout.data_ptr(), _ptr(plse))
+    db = _Decode(dq.data_ptr(), decode["block_tables"].data_ptr(), decode["block_starts"].data_ptr(),
+                 decode["seq_lens"].data_ptr(), decode["q_pos"].data_ptr(), dq.shape[0],
+                 decode["block_tables"].shape[1], dout.data_ptr(), _ptr(dlse))
+    if workspace is None:
+        n = decode_workspace_size(dq.shape[0], Hq, kv.num_kv_heads, kv.head_dim, decode["block_tables"].shape[1],
+                                  kv.block_size)
+        workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=dq.device)
+    rp = _Rope(rope.data_ptr(), rope.shape[0], rope.shape[1])
+    st = L.minipic_attn_mixed(_dtype_code(pq), Hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(pb),
+                              ctypes.byref(db), float(scale), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "minipic_attn_mixed")
+    return pout, plse, dout, dlse
 
 
 def device_error(clear: bool = True, stream=None) -> int:

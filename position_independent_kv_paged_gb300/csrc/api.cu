@@ -51,17 +51,8 @@ int current_sms() {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-struct DecodeWs {
-  size_t o_bytes, ml_bytes, total;
-};
-
-DecodeWs decode_ws(int batch, int Hq, int D, int n_split) {
-  DecodeWs w{0, 0, 0};
-  if (n_split <= 1) return w;
-  w.o_bytes = align_up((size_t)batch * Hq * n_split * D * sizeof(float), 256);
-  w.ml_bytes = align_up((size_t)batch * Hq * n_split * 2 * sizeof(float), 256);
-  w.total = w.o_bytes + w.ml_bytes;
-  return w;
+DecodeWs decode_ws(int batch, int Hq, int Hkv, int D, int n_split) {
+  return decode_ws_layout(batch, Hq, Hkv, D, n_split);
 }
 
 minipic_status check_pool(const minipic_kv_pool* kv, int32_t num_q_heads, bool need_ptrs) {
@@ -86,10 +77,12 @@ minipic_status check_rope(const minipic_rope* rope, int head_dim) {
   return MINIPIC_OK;
 }
 
-minipic_status decode_common(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
-                             const minipic_rope* rope, const minipic_decode_batch* b, float scale,
-                             void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                             bool rotate) {
+// Validate a decode batch and fill the launch arguments (no launch).
+minipic_status build_decode(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                            const minipic_rope* rope, const minipic_decode_batch* b, float scale, void* workspace,
+                            size_t workspace_bytes, bool rotate, DecodeArgs* out_args, DecodePlan* out_plan,
+                            bool* empty) {
+  *empty = false;
   if (dtype != MINIPIC_F32 && dtype != MINIPIC_BF16) return MINIPIC_ERR_INVALID;
   if (!b) return MINIPIC_ERR_INVALID;
   minipic_status st = check_pool(kv, num_q_heads, b->batch > 0);
@@ -99,7 +92,10 @@ minipic_status decode_common(minipic_dtype dtype, int32_t num_q_heads, const min
     st = check_rope(rope, kv->head_dim);
     if (st != MINIPIC_OK) return st;
   }
-  if (b->batch == 0) return MINIPIC_OK;
+  if (b->batch == 0) {
+    *empty = true;
+    return MINIPIC_OK;
+  }
   if (b->max_blocks_per_seq == 0) return MINIPIC_ERR_INVALID;
   if (!b->q || !b->block_tables || !b->block_starts || !b->seq_lens || !b->q_pos || !b->out)
     return MINIPIC_ERR_INVALID;
@@ -115,7 +111,7 @@ minipic_status decode_common(minipic_dtype dtype, int32_t num_q_heads, const min
   const int G = num_q_heads / kv->num_kv_heads;
   DecodePlan plan = plan_decode(b->batch, kv->num_kv_heads, G, kv->head_dim, b->max_blocks_per_seq,
                                 kv->block_size, bf16, sms);
-  DecodeWs ws = decode_ws(b->batch, num_q_heads, kv->head_dim, plan.n_split);
+  DecodeWs ws = decode_ws(b->batch, num_q_heads, kv->num_kv_heads, kv->head_dim, plan.n_split);
   if (ws.total > 0) {
     if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return MINIPIC_ERR_WORKSPACE;
   }
@@ -132,8 +128,10 @@ minipic_status decode_common(minipic_dtype dtype, int32_t num_q_heads, const min
   a.max_pos = rotate ? rope->max_pos : 0;
   a.out = b->out;
   a.lse = b->lse;
-  a.part_o = ws.total ? static_cast<float*>(workspace) : nullptr;
-  a.part_ml = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_bytes) : nullptr;
+  char* wsb = static_cast<char*>(workspace);
+  a.counters = ws.total ? reinterpret_cast<int*>(wsb) : nullptr;
+  a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.cnt_bytes) : nullptr;
+  a.part_ml = ws.total ? reinterpret_cast<float*>(wsb + ws.cnt_bytes + ws.o_bytes) : nullptr;
   a.batch = b->batch;
   a.Hq = num_q_heads;
   a.Hkv = kv->num_kv_heads;
@@ -146,11 +144,101 @@ minipic_status decode_common(minipic_dtype dtype, int32_t num_q_heads, const min
   a.n_split = plan.n_split;
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)kv->head_dim);
   a.err = err;
-  cudaError_t e = launch_decode(a, bf16, rotate, plan, stream);
+  *out_args = a;
+  *out_plan = plan;
+  return MINIPIC_OK;
+}
+
+minipic_status decode_common(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                             const minipic_rope* rope, const minipic_decode_batch* b, float scale,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream, bool rotate) {
+  DecodeArgs a{};
+  DecodePlan plan{};
+  bool empty = false;
+  const minipic_status st =
+      build_decode(dtype, num_q_heads, kv, rope, b, scale, workspace, workspace_bytes, rotate, &a, &plan, &empty);
+  if (st != MINIPIC_OK || empty) return st;
+  const cudaError_t e = launch_decode(a, dtype == MINIPIC_BF16, rotate, plan, stream);
+  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
+// Validate a prefill batch and fill the launch arguments (no launch).
+minipic_status build_prefill(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                             const minipic_rope* rope, const minipic_prefill_batch* b, float scale, bool rotate,
+                             PrefillArgs* out_args, bool* empty) {
+  *empty = false;
+  if (dtype != MINIPIC_F32 && dtype != MINIPIC_BF16) return MINIPIC_ERR_INVALID;
+  if (!b) return MINIPIC_ERR_INVALID;
+  minipic_status st = check_pool(kv, num_q_heads, b->batch > 0);
+  if (st != MINIPIC_OK) return st;
+  if (rotate) {
+    st = check_rope(rope, kv->head_dim);
+    if (st != MINIPIC_OK) return st;
+  }
+  if (dtype != MINIPIC_BF16) return MINIPIC_ERR_UNSUPPORTED;
+  if (b->batch < 0 || b->total_q < 0 || b->max_q_len < 0 || b->max_blocks_per_seq < 0) return MINIPIC_ERR_INVALID;
+  if (b->batch == 0 || b->total_q == 0) {
+    *empty = true;
+    return MINIPIC_OK;
+  }
+  if (b->max_q_len == 0 || b->max_blocks_per_seq == 0 || kv->num_blocks == 0) return MINIPIC_ERR_INVALID;
+  if (!b->q || !b->cu_q_lens || !b->q_pos || !b->block_tables || !b->block_starts || !b->kv_lens || !b->out)
+    return MINIPIC_ERR_INVALID;
+  if (!aligned16(b->q) || !aligned16(b->out)) return MINIPIC_ERR_INVALID;
+  if (!isfinite(scale)) return MINIPIC_ERR_INVALID;
+  int* err = nullptr;
+  if (device_info(&err, nullptr) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  PrefillArgs a{};
+  a.q = b->q;
+  a.cu_q_lens = b->cu_q_lens;
+  a.q_pos = b->q_pos;
+  a.k_pool = kv->k_pool;
+  a.v_pool = kv->v_pool;
+  a.block_tables = b->block_tables;
+  a.block_starts = b->block_starts;
+  a.kv_lens = b->kv_lens;
+  a.cos_sin = rotate ? rope->cos_sin : nullptr;
+  a.max_pos = rotate ? rope->max_pos : 0;
+  a.out = b->out;
+  a.lse = b->lse;
+  a.batch = b->batch;
+  a.total_q = b->total_q;
+  a.max_q_len = b->max_q_len;
+  a.Hq = num_q_heads;
+  a.Hkv = kv->num_kv_heads;
+  a.G = num_q_heads / kv->num_kv_heads;
+  a.D = kv->head_dim;
+  a.BS = kv->block_size;
+  a.num_blocks = kv->num_blocks;
+  a.max_blocks = b->max_blocks_per_seq;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)kv->head_dim);
+  a.err = err;
+  *out_args = a;
+  return MINIPIC_OK;
+}
+
+minipic_status prefill_common(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                              const minipic_rope* rope, const minipic_prefill_batch* b, float scale,
+                              cudaStream_t stream, bool rotate) {
+  PrefillArgs a{};
+  bool empty = false;
+  const minipic_status st = build_prefill(dtype, num_q_heads, kv, rope, b, scale, rotate, &a, &empty);
+  if (st != MINIPIC_OK || empty) return st;
+  const cudaError_t e = launch_prefill_tc(a, rotate, stream);
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 
 }  // namespace
+
+DecodeWs decode_ws_layout(int batch, int Hq, int Hkv, int D, int n_split) {
+  DecodeWs w{0, 0, 0, 0};
+  if (n_split <= 1) return w;
+  w.cnt_bytes = align_up((size_t)batch * Hkv * sizeof(int), 256);
+  w.o_bytes = align_up((size_t)batch * Hq * n_split * D * sizeof(float), 256);
+  w.ml_bytes = align_up((size_t)batch * Hq * n_split * 2 * sizeof(float), 256);
+  w.total = w.cnt_bytes + w.o_bytes + w.ml_bytes;
+  return w;
+}
 
 DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs, bool bf16, int num_sms) {
   (void)D;
@@ -186,7 +274,9 @@ DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs,
 
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, bool rotate, const DecodePlan& plan,
                           cudaStream_t s) {
-  cudaError_t e = plan.use_mma ? launch_decode_mma(a, rotate, s) : launch_decode_simt(a, bf16, rotate, s);
+  // the tensor-core kernel merges its splits itself; the SIMT path merges in a second kernel
+  if (plan.use_mma) return launch_decode_mma(a, rotate, s);
+  cudaError_t e = launch_decode_simt(a, bf16, rotate, s);
   if (e != cudaSuccess) return e;
   return launch_decode_merge(a, bf16, s);
 }
@@ -229,8 +319,8 @@ size_t minipic_attn_decode_workspace_size(int32_t batch, int32_t num_q_heads, in
                              current_sms());
   DecodePlan p32 = plan_decode(batch, num_kv_heads, G, head_dim, max_blocks_per_seq, block_size, false,
                                current_sms());
-  const size_t a = decode_ws(batch, num_q_heads, head_dim, p.n_split).total;
-  const size_t b = decode_ws(batch, num_q_heads, head_dim, p32.n_split).total;
+  const size_t a = decode_ws(batch, num_q_heads, num_kv_heads, head_dim, p.n_split).total;
+  const size_t b = decode_ws(batch, num_q_heads, num_kv_heads, head_dim, p32.n_split).total;
   return a > b ? a : b;
 }
 
@@ -253,64 +343,6 @@ size_t minipic_attn_prefill_workspace_size(int32_t, int32_t, int32_t, int32_t, i
   return 0;
 }
 
-}  // extern "C"
-
-namespace {
-
-minipic_status prefill_common(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
-                              const minipic_rope* rope, const minipic_prefill_batch* b, float scale,
-                              cudaStream_t stream, bool rotate) {
-  if (dtype != MINIPIC_F32 && dtype != MINIPIC_BF16) return MINIPIC_ERR_INVALID;
-  if (!b) return MINIPIC_ERR_INVALID;
-  minipic_status st = check_pool(kv, num_q_heads, b->batch > 0);
-  if (st != MINIPIC_OK) return st;
-  if (rotate) {
-    st = check_rope(rope, kv->head_dim);
-    if (st != MINIPIC_OK) return st;
-  }
-  if (dtype != MINIPIC_BF16) return MINIPIC_ERR_UNSUPPORTED;
-  if (b->batch < 0 || b->total_q < 0 || b->max_q_len < 0 || b->max_blocks_per_seq < 0) return MINIPIC_ERR_INVALID;
-  if (b->batch == 0 || b->total_q == 0) return MINIPIC_OK;
-  if (b->max_q_len == 0 || b->max_blocks_per_seq == 0 || kv->num_blocks == 0) return MINIPIC_ERR_INVALID;
-  if (!b->q || !b->cu_q_lens || !b->q_pos || !b->block_tables || !b->block_starts || !b->kv_lens || !b->out)
-    return MINIPIC_ERR_INVALID;
-  if (!aligned16(b->q) || !aligned16(b->out)) return MINIPIC_ERR_INVALID;
-  if (!isfinite(scale)) return MINIPIC_ERR_INVALID;
-  int* err = nullptr;
-  if (device_info(&err, nullptr) != cudaSuccess) return MINIPIC_ERR_CUDA;
-  PrefillArgs a{};
-  a.q = b->q;
-  a.cu_q_lens = b->cu_q_lens;
-  a.q_pos = b->q_pos;
-  a.k_pool = kv->k_pool;
-  a.v_pool = kv->v_pool;
-  a.block_tables = b->block_tables;
-  a.block_starts = b->block_starts;
-  a.kv_lens = b->kv_lens;
-  a.cos_sin = rotate ? rope->cos_sin : nullptr;
-  a.max_pos = rotate ? rope->max_pos : 0;
-  a.out = b->out;
-  a.lse = b->lse;
-  a.batch = b->batch;
-  a.total_q = b->total_q;
-  a.max_q_len = b->max_q_len;
-  a.Hq = num_q_heads;
-  a.Hkv = kv->num_kv_heads;
-  a.G = num_q_heads / kv->num_kv_heads;
-  a.D = kv->head_dim;
-  a.BS = kv->block_size;
-  a.num_blocks = kv->num_blocks;
-  a.max_blocks = b->max_blocks_per_seq;
-  a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)kv->head_dim);
-  a.err = err;
-  const cudaError_t e = launch_prefill_tc(a, rotate, stream);
-  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
-}
-
-}  // namespace
-
-extern "C" {
-
 minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
                                     const minipic_rope* rope, const minipic_prefill_batch* batch, float scale,
                                     void* workspace, size_t workspace_bytes, minipic_stream_t stream) {
@@ -323,6 +355,33 @@ minipic_status minipic_attn_prefill_prerotated(minipic_dtype dtype, int32_t num_
                                                const minipic_prefill_batch* batch, float scale,
                                                minipic_stream_t stream) {
   return prefill_common(dtype, num_q_heads, kv, nullptr, batch, scale, (cudaStream_t)stream, false);
+}
+
+minipic_status minipic_attn_mixed(minipic_dtype dtype, int32_t num_q_heads, const minipic_kv_pool* kv,
+                                  const minipic_rope* rope, const minipic_prefill_batch* prefill,
+                                  const minipic_decode_batch* decode, float scale, void* workspace,
+                                  size_t workspace_bytes, minipic_stream_t stream) {
+  if (dtype != MINIPIC_BF16) return (dtype == MINIPIC_F32) ? MINIPIC_ERR_UNSUPPORTED : MINIPIC_ERR_INVALID;
+  PrefillArgs p{};
+  DecodeArgs d{};
+  DecodePlan plan{};
+  bool p_empty = false, d_empty = false;
+  minipic_status st = build_prefill(dtype, num_q_heads, kv, rope, prefill, scale, true, &p, &p_empty);
+  if (st != MINIPIC_OK) return st;
+  st = build_decode(dtype, num_q_heads, kv, rope, decode, scale, workspace, workspace_bytes, true, &d, &plan,
+                    &d_empty);
+  if (st != MINIPIC_OK) return st;
+  cudaError_t e = cudaSuccess;
+  if (p_empty && d_empty) return MINIPIC_OK;
+  if (d_empty) {
+    e = launch_prefill_tc(p, true, (cudaStream_t)stream);
+  } else if (p_empty) {
+    e = launch_decode(d, true, true, plan, (cudaStream_t)stream);
+  } else {
+    if (kv->num_blocks == 0) return MINIPIC_ERR_INVALID;
+    e = launch_mixed(p, d, (cudaStream_t)stream);
+  }
+  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 
 minipic_status minipic_device_error(int32_t* flags_out, int32_t clear, minipic_stream_t stream) {

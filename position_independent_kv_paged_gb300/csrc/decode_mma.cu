@@ -1,579 +1,26 @@
-// Decode attention over the position-free paged cache, bf16 tensor-core form.
-//
-// Method (MiniPIC summary, gist.science 2606.13126, section 2.1): keys are
-// stored unrotated; the kernel rotates them at their logical position
-// pi(j) = start[r][block] + slot with a cos/sin table lookup and multiply-adds
-// per key element, then runs ordinary softmax attention.
-//
-// Layout of the work.  One CTA = (split, kv head, request); each of its 4 warps
-// owns every 4th block of the split and runs its own 3-stage TMA pipeline: the
-// (block, head) K and V tiles (16 keys x d, contiguous in the pool) arrive by
-// cp.async.bulk.tensor with 128-byte swizzle, in a [half][key][64] shared
-// layout that makes both the 16-byte key-row reads and the transposing
-// ldmatrix reads of V free of bank conflicts.
-//
-// Per 16-key block and GQA group (up to 8 query heads per n-tile):
-//   S^T[key][head] = K'[key][:] . Q'[head][:]  (mma m16n8k16, M = the 16 keys)
-//   O^T[dim][head] += V^T[dim][key] P^T[key][head]
-// K' is formed in registers: rows are read from shared memory, rotated in
-// fp32 with two multiply-adds per element, and packed to bf16 as the MMA's A
-// operand.  The contraction order of the head dimension is a per-thread
-// permutation chosen so that each rotary pair (i, i + d/2) is thread-local;
-// Q' uses the same permutation.
-//
-// Rotation is factored per block: with s = slot and b = block start,
-//   (R_t q)^T (R_{b+s} k~) = (R_{t-b} q)^T (R_s k~),
-// so q is re-rotated once per block by the table row |t - b| (sin negated for
-// t < b) and each key row by the constant R_s (s < 16) held in registers.
-// This is the same algebra as rotating k~ by R_{pi(j)}; it reads one 512-byte
-// table row per block instead of sixteen.
-#include <cudaTypedefs.h>
-#include <math_constants.h>
-
-#include <mutex>
-
-#include "internal.h"
-#include "ptx.cuh"
+// Decode kernel wrapper and launcher (the CTA body is in decode_body.cuh).
+#include "decode_body.cuh"
+#include "tmap.cuh"
 
 namespace minipic {
 namespace {
 
-using ptx::U4;
-
-constexpr int kWarps = 4;
-constexpr int kStages = 3;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-
-template <int D>
-struct Geo {
-  static constexpr int TILE = 16 * D * 2;     // bytes of one (block, head) tile of K or V
-  static constexpr int NCH = D / 32;          // 16-byte chunks of a key row read by one thread
-  static constexpr int NPAIR = NCH / 2;       // rotary chunk pairs per row and thread
-  static constexpr int MT = D / 16;           // m-tiles of O^T
-  static constexpr int HALVES = D / 64;       // 128-byte halves of a key row
-  static constexpr int STAGE = 2 * TILE;
-};
-
-// Which 16-byte chunk (0..7 within a 128-byte half) and which half thread
-// `tig` reads as its i-th chunk of a key row, and the rotary pairing: thread
-// tig owns chunks tig and tig + 4 of every half, so each rotary pair
-// (i, i + d/2) is thread-local and every shared read below is conflict-free.
-template <int D>
-struct Chunks {
-  int c[Geo<D>::NCH];
-  int h[Geo<D>::NCH];
-  int first[Geo<D>::NPAIR], second[Geo<D>::NPAIR];
-  int fbase[Geo<D>::NPAIR];  // first frequency index of the pair's 8 elements
-  __device__ __forceinline__ explicit Chunks(int tig) {
-    if constexpr (D == 128) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        h[i] = i >> 1;
-        c[i] = tig + 4 * (i & 1);
-      }
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        first[p] = p;
-        second[p] = p + 2;
-        fbase[p] = 8 * (tig + 4 * p);
-      }
-    } else {
-      c[0] = tig;
-      c[1] = tig + 4;
-      h[0] = h[1] = 0;
-      first[0] = 0;
-      second[0] = 1;
-      fbase[0] = 8 * tig;
-    }
-  }
-};
-
-// Physical key (slot) held by MMA fragment row g (g < 8; row g + 8 holds
-// slot + 8).  Rows read together by a quarter warp then differ in bit 2 of the
-// slot, which keeps the swizzled key-row reads conflict-free.
-__device__ __forceinline__ int frag_slot(int g) { return (g >> 1) | ((g & 1) << 2); }
-
-// Byte offset of (half, key, chunk) in a swizzled [half][16 keys][128 B] tile.
-__device__ __forceinline__ uint32_t swz(int half, int key, int chunk) {
-  return (uint32_t)((half * 16 + key) * 128 + ((chunk ^ (key & 7)) << 4));
-}
-
-// Rotate one pair of 8-element bf16 chunks in fp32 (packed pairs) and repack:
-//   x' = x c - y s,  y' = y c + x s   (s already carries the pair's sign)
-// c2/s2 hold the 8 cosines/sines as 4 packed fp32 pairs.
-__device__ __forceinline__ void rotate_pair(U4& x, U4& y, const uint64_t (&c2)[4], const uint64_t (&s2)[4]) {
-  uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-  uint32_t yw[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint64_t xv = ptx::bf2_to_f2(xw[k]), yv = ptx::bf2_to_f2(yw[k]);
-    const uint64_t xn = ptx::sub2(ptx::mul2(xv, c2[k]), ptx::mul2(yv, s2[k]));
-    const uint64_t yn = ptx::fma2(xv, s2[k], ptx::mul2(yv, c2[k]));
-    xw[k] = ptx::f2_to_bf2(xn);
-    yw[k] = ptx::f2_to_bf2(yn);
-  }
-  x = U4{xw[0], xw[1], xw[2], xw[3]};
-  y = U4{yw[0], yw[1], yw[2], yw[3]};
-}
-
-__device__ __forceinline__ uint32_t w_of(const U4& v, int k) {
-  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
-}
-
-// Shared-memory plan of one CTA (offsets from a 1024-byte aligned base).
-template <int D>
-struct Smem {
-  static constexpr int STAGES = kWarps * kStages * Geo<D>::STAGE;  // K|V tiles
-  static constexpr int ROWB = 4 * D;                               // one cos|sin table row
-  static constexpr int ROWS = STAGES;                              // [warp][stage] table rows
-  static constexpr int META = ROWS + kWarps * kStages * ROWB;      // [split block][phys, start]
-  static constexpr int kMaxSplit = 512;                            // split_blocks cap (planner)
-  static constexpr int BARS = META + kMaxSplit * 8;
-  static constexpr int TOTAL = BARS + kWarps * kStages * 8;
-};
+using namespace decode_impl;
 
 template <int D, int NT, bool ROPE>
 __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const DecodeArgs a) {
-  using GE = Geo<D>;
-  using SM = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
-  uint8_t* sgen = smem_raw + (sbase - ptx::smem_addr(smem_raw));
-  const uint32_t bar_base = sbase + SM::BARS;
-  int* meta = reinterpret_cast<int*>(sgen + SM::META);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g8 = lane >> 2, tig = lane & 3;
-  const int split = blockIdx.x, hk = blockIdx.y, r = blockIdx.z;
-  const int G = a.G;
-  const int mb = a.max_blocks;
-
-  int L = a.seq_lens[r];
-  const int Lmax = mb * 16;
-  if (L < 0 || L > Lmax) {
-    if (threadIdx.x == 0 && split == 0) atomicOr(a.err, kErrSeqLen);
-    L = L < 0 ? 0 : Lmax;
-  }
-  const int nblk = (L + 15) >> 4;
-  const int n_valid = max(1, (nblk + a.split_blocks - 1) / a.split_blocks);
-  if (split >= n_valid) return;
-  const int b_begin = split * a.split_blocks;
-  const int b_end = min(nblk, b_begin + a.split_blocks);
-  const int span = b_end - b_begin;
-  const int nmine = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
-
-  // block ids and start positions of the whole split, staged once
-  {
-    const int* bt = a.block_tables + (size_t)r * mb + b_begin;
-    const int* bs_ = a.block_starts + (size_t)r * mb + b_begin;
-    for (int i = threadIdx.x; i < span; i += blockDim.x) {
-      meta[2 * i] = __ldg(bt + i);
-      meta[2 * i + 1] = ROPE ? __ldg(bs_ + i) : 0;
-    }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int st = 0; st < kStages; ++st) ptx::mbar_init(bar_base + (warp * kStages + st) * 8, 1);
-    ptx::fence_barrier_init();
-    ptx::fence_proxy_async_smem();
-  }
-
-  const Chunks<D> ch(tig);
-  const int ks0 = frag_slot(g8);  // this thread's key rows: slots ks0 and ks0 + 8
-
-  // unrotated queries of this thread's heads (g8 + 8 nt), in the thread's chunk order
-  U4 qraw[NT][GE::NCH];
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int head = 8 * nt + g8;
-#pragma unroll
-    for (int i = 0; i < GE::NCH; ++i) {
-      if (head < G) {
-        const __nv_bfloat16* p = qg + ((size_t)r * a.Hq + (size_t)hk * G + head) * D + 64 * ch.h[i] + 8 * ch.c[i];
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-        qraw[nt][i] = U4{v.x, v.y, v.z, v.w};
-      } else {
-        qraw[nt][i] = U4{0u, 0u, 0u, 0u};
-      }
-    }
-  }
-  const float qs = a.scale * kLog2e;  // applied to the scores; softmax runs in base 2
-
-  // R_s for the two key rows (slots g8, g8 + 8) of this thread, as packed pairs
-  uint64_t rsc[2][GE::NPAIR][4], rss[2][GE::NPAIR][4];
-  int tq = 0;
-  if constexpr (ROPE) {
-#pragma unroll
-    for (int row = 0; row < 2; ++row) {
-      const int srow = min(ks0 + 8 * row, a.max_pos - 1);
-      const float* t = a.cos_sin + (size_t)srow * D;
-#pragma unroll
-      for (int p = 0; p < GE::NPAIR; ++p) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 c = __ldg(reinterpret_cast<const float2*>(t + ch.fbase[p] + 2 * e));
-          const float2 sn = __ldg(reinterpret_cast<const float2*>(t + D / 2 + ch.fbase[p] + 2 * e));
-          rsc[row][p][e] = ptx::f2(c.x, c.y);
-          rss[row][p][e] = ptx::f2(sn.x, sn.y);
-        }
-      }
-    }
-    tq = a.q_pos[r];
-    if (tq < 0 || tq >= a.max_pos) {
-      if (threadIdx.x == 0 && split == 0) atomicOr(a.err, kErrPosition);
-      tq = 0;
-    }
-  }
-  U4 qw[NT][GE::NCH];
-  if constexpr (!ROPE) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < GE::NCH; ++i) qw[nt][i] = qraw[nt][i];
-  }
-
-  float mrun[NT][2], lrun[NT][2];
-  float oacc[GE::MT][NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    mrun[nt][0] = mrun[nt][1] = -CUDART_INF_F;
-    lrun[nt][0] = lrun[nt][1] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < GE::MT; ++mt)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) oacc[mt][nt][k] = 0.f;
-  }
-
-  __syncthreads();  // meta visible, barriers initialised
-
-  // lane 0: issue the k-th block of this warp into its stage: K and V tiles by
-  // TMA, plus the table row |t - start| the block's query rotation needs
-  auto issue = [&](int k) {
-    const int i = warp + kWarps * k;
-    const int stg = k % kStages;
-    const uint32_t bar = bar_base + (warp * kStages + stg) * 8;
-    const uint32_t kdst = sbase + (warp * kStages + stg) * GE::STAGE;
-    const int phys = meta[2 * i];
-    if (phys < 0 || phys >= a.num_blocks) {
-      ptx::mbar_arrive(bar);  // nothing to load; the consumer masks the block
-      return;
-    }
-    int ad = 0;
-    bool row_ok = false;
-    if constexpr (ROPE) {
-      const int delta = tq - meta[2 * i + 1];
-      ad = delta < 0 ? -delta : delta;
-      row_ok = ad < a.max_pos;
-    }
-    ptx::mbar_arrive_expect_tx(bar, 2 * GE::TILE + (row_ok ? SM::ROWB : 0));
-    const int y = (phys * a.Hkv + hk) * 16;
-#pragma unroll
-    for (int hh = 0; hh < GE::HALVES; ++hh) {
-      ptx::tma_load_2d(kdst + hh * 2048, &kmap, 64 * hh, y, bar);
-      ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
-    }
-    if (row_ok)
-      ptx::bulk_load(sbase + SM::ROWS + (warp * kStages + stg) * SM::ROWB, a.cos_sin + (size_t)ad * D, SM::ROWB,
-                     bar);
-  };
-  if (lane == 0) {
-    const int pre = nmine < kStages ? nmine : kStages;
-    for (int k = 0; k < pre; ++k) issue(k);
-  }
-
-  bool timed_out = false;
-  int k_stop = nmine;
-  for (int k = 0; k < nmine; ++k) {
-    const int i = warp + kWarps * k;
-    const int b = b_begin + i;
-    const int stg = k % kStages;
-    const uint32_t bar = bar_base + (warp * kStages + stg) * 8;
-    const uint32_t kbase = sbase + (warp * kStages + stg) * GE::STAGE;
-    const uint32_t vbase = kbase + GE::TILE;
-    const uint32_t rowb = sbase + SM::ROWS + (warp * kStages + stg) * SM::ROWB;
-
-    const int phys = meta[2 * i];
-    const bool ok = phys >= 0 && phys < a.num_blocks;
-    const int start = meta[2 * i + 1];
-    const int nk = min(16, L - b * 16);
-    bool v0 = ok && ks0 < nk, v1 = ok && ks0 + 8 < nk;
-    if (!ok && lane == 0) atomicOr(a.err, kErrBlockId);
-    int delta = 0;
-    if constexpr (ROPE) {
-      delta = tq - start;
-      const int ad = delta < 0 ? -delta : delta;
-      if (ok && !(ad < a.max_pos && start >= 0 && start + nk - 1 < a.max_pos)) {
-        // keys whose position falls outside the table are masked
-        const bool p0 = start + ks0 >= 0 && start + ks0 < a.max_pos && ad < a.max_pos;
-        const bool p1 = start + ks0 + 8 >= 0 && start + ks0 + 8 < a.max_pos && ad < a.max_pos;
-        if (__any_sync(0xffffffffu, (v0 && !p0) || (v1 && !p1)) && lane == 0) atomicOr(a.err, kErrPosition);
-        v0 = v0 && p0;
-        v1 = v1 && p1;
-      }
-    }
-
-    // wait for this block's tiles (bounded)
-    const bool arrived = ptx::mbar_wait(bar, (uint32_t)((k / kStages) & 1));
-    if (!__all_sync(0xffffffffu, arrived)) {
-      if (lane == 0) atomicOr(a.err, kErrTimeout);
-      timed_out = true;
-      k_stop = k;
-      break;
-    }
-
-    // re-rotate q by t - start from the staged table row
-    if constexpr (ROPE) {
-      const float sg = delta < 0 ? -1.f : 1.f;
-#pragma unroll
-      for (int p = 0; p < GE::NPAIR; ++p) {
-        const U4 c0 = ptx::lds128(rowb + 4 * ch.fbase[p]);
-        const U4 c1 = ptx::lds128(rowb + 4 * ch.fbase[p] + 16);
-        const U4 s0 = ptx::lds128(rowb + 2 * D + 4 * ch.fbase[p]);
-        const U4 s1 = ptx::lds128(rowb + 2 * D + 4 * ch.fbase[p] + 16);
-        uint64_t c2[4], s2[4];
-        c2[0] = ptx::f2(__uint_as_float(c0.x), __uint_as_float(c0.y));
-        c2[1] = ptx::f2(__uint_as_float(c0.z), __uint_as_float(c0.w));
-        c2[2] = ptx::f2(__uint_as_float(c1.x), __uint_as_float(c1.y));
-        c2[3] = ptx::f2(__uint_as_float(c1.z), __uint_as_float(c1.w));
-        s2[0] = ptx::f2(sg * __uint_as_float(s0.x), sg * __uint_as_float(s0.y));
-        s2[1] = ptx::f2(sg * __uint_as_float(s0.z), sg * __uint_as_float(s0.w));
-        s2[2] = ptx::f2(sg * __uint_as_float(s1.x), sg * __uint_as_float(s1.y));
-        s2[3] = ptx::f2(sg * __uint_as_float(s1.z), sg * __uint_as_float(s1.w));
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          U4 x = qraw[nt][ch.first[p]], y = qraw[nt][ch.second[p]];
-          rotate_pair(x, y, c2, s2);
-          qw[nt][ch.first[p]] = x;
-          qw[nt][ch.second[p]] = y;
-        }
-      }
-    }
-
-    // key rows g8 and g8 + 8 of the block, rotated by R_slot in registers
-    U4 kr[2][GE::NCH];
-#pragma unroll
-    for (int row = 0; row < 2; ++row)
-#pragma unroll
-      for (int c = 0; c < GE::NCH; ++c) kr[row][c] = ptx::lds128(kbase + swz(ch.h[c], ks0 + 8 * row, ch.c[c]));
-    if constexpr (ROPE) {
-#pragma unroll
-      for (int row = 0; row < 2; ++row)
-#pragma unroll
-        for (int p = 0; p < GE::NPAIR; ++p)
-          rotate_pair(kr[row][ch.first[p]], kr[row][ch.second[p]], rsc[row][p], rss[row][p]);
-    }
-
-    // S^T = K' Q'^T, two independent accumulation chains (even / odd k-steps)
-    float sacc[NT][4], sacc2[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[nt][e] = sacc2[nt][e] = 0.f;
-#pragma unroll
-    for (int c = 0; c < GE::NCH; ++c) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t a0 = w_of(kr[0][c], 2 * u), a1 = w_of(kr[1][c], 2 * u);
-        const uint32_t a2 = w_of(kr[0][c], 2 * u + 1), a3 = w_of(kr[1][c], 2 * u + 1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          if (u == 0)
-            ptx::mma_bf16_16816(sacc[nt], a0, a1, a2, a3, w_of(qw[nt][c], 0), w_of(qw[nt][c], 1));
-          else
-            ptx::mma_bf16_16816(sacc2[nt], a0, a1, a2, a3, w_of(qw[nt][c], 2), w_of(qw[nt][c], 3));
-        }
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
-
-    // online softmax over the 16 keys, per head column (2 tig + j) of each n-tile
-    uint32_t pb0[NT], pb1[NT];
-    float corr[NT][2];
-    bool any_corr = false;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float pv[4];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float sa = v0 ? sacc[nt][j] * qs : -CUDART_INF_F;
-        const float sb = v1 ? sacc[nt][2 + j] * qs : -CUDART_INF_F;
-        float bm = fmaxf(sa, sb);
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-        const float mnew = fmaxf(mrun[nt][j], bm);
-        const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
-        corr[nt][j] = exp2f(mrun[nt][j] - muse);
-        any_corr |= mnew != mrun[nt][j];
-        const float pa = exp2f(sa - muse), pbv = exp2f(sb - muse);
-        lrun[nt][j] = fmaf(lrun[nt][j], corr[nt][j], pa + pbv);
-        mrun[nt][j] = mnew;
-        pv[j] = pa;
-        pv[2 + j] = pbv;
-      }
-      pb0[nt] = ptx::movmatrix_trans(ptx::pack_bf16(pv[0], pv[1]));  // keys 0..7
-      pb1[nt] = ptx::movmatrix_trans(ptx::pack_bf16(pv[2], pv[3]));  // keys 8..15
-    }
-    // rescale the accumulators only when some running max moved
-    if (__any_sync(0xffffffffu, any_corr)) {
-#pragma unroll
-      for (int mt = 0; mt < GE::MT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            oacc[mt][nt][j] *= corr[nt][j];
-            oacc[mt][nt][2 + j] *= corr[nt][j];
-          }
-    }
-
-    // O^T += V^T P^T
-    {
-      const int mi = lane >> 3, rr = lane & 7;
-      const int key = frag_slot(rr) + 8 * (mi >> 1);
-#pragma unroll
-      for (int mt = 0; mt < GE::MT; ++mt) {
-        const int cg = 2 * mt + (mi & 1);
-        uint32_t a0, a1, a2, a3;
-        ptx::ldsm_x4_trans(vbase + swz(cg >> 3, key, cg & 7), a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) ptx::mma_bf16_16816(oacc[mt][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
-      }
-    }
-
-    __syncwarp();
-    if (lane == 0 && k + kStages < nmine) issue(k + kStages);
-  }
-
-  if (timed_out) {
-    // blocks k_stop .. k_stop + kStages - 1 were issued and not consumed
-    if (lane == 0) {
-      const int last = min(nmine, k_stop + kStages);
-      for (int k2 = k_stop; k2 < last; ++k2) {
-        const int stg = k2 % kStages;
-        ptx::mbar_wait(bar_base + (warp * kStages + stg) * 8, (uint32_t)((k2 / kStages) & 1), 100000000ull);
-      }
-    }
-  }
-
-  // per-warp state -> this warp's own stage region: m[16], l[16], O[16][D + 4]
-  constexpr int OST = D + 4;  // padded row stride (conflict-free stores)
-  float* wm = reinterpret_cast<float*>(sgen + warp * kStages * GE::STAGE);
-  float* wl = wm + 16;
-  float* wo = wm + 32;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float l = lrun[nt][j];
-      l += __shfl_xor_sync(0xffffffffu, l, 4);
-      l += __shfl_xor_sync(0xffffffffu, l, 8);
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      lrun[nt][j] = l;
-    }
-  __syncwarp();
-  if (g8 == 0) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        wm[8 * nt + 2 * tig + j] = mrun[nt][j];
-        wl[8 * nt + 2 * tig + j] = lrun[nt][j];
-      }
-  }
-#pragma unroll
-  for (int mt = 0; mt < GE::MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int head = 8 * nt + 2 * tig + j;
-        wo[head * OST + 16 * mt + g8] = oacc[mt][nt][j];
-        wo[head * OST + 16 * mt + g8 + 8] = oacc[mt][nt][2 + j];
-      }
-  __syncthreads();
-
-  const bool direct = (n_valid == 1);
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int head = idx / D, dim = idx - head * D;
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-      M = fmaxf(M, reinterpret_cast<const float*>(sgen + w * kStages * GE::STAGE)[head]);
-    float Ls = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float* base = reinterpret_cast<const float*>(sgen + w * kStages * GE::STAGE);
-      const float mw = base[head];
-      const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
-      Ls = fmaf(base[16 + head], f, Ls);
-      O = fmaf(base[32 + head * OST + dim], f, O);
-    }
-    const int hq = hk * G + head;
-    if (direct) {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((size_t)r * a.Hq + hq) * D + dim;
-      *out = __float2bfloat16_rn(Ls > 0.f ? O / Ls : 0.f);
-      if (dim == 0 && a.lse) a.lse[(size_t)r * a.Hq + hq] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
-    } else {
-      const size_t pi = ((size_t)r * a.Hq + hq) * a.n_split + split;
-      a.part_o[pi * D + dim] = O;
-      if (dim == 0) {
-        a.part_ml[pi * 2] = M;
-        a.part_ml[pi * 2 + 1] = Ls;
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------- host side
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// 2-D view [rows = num_blocks * Hkv * 16][D] of a bf16 pool; box = 64 x 16, 128-byte swizzle.
-bool make_pool_map(CUtensorMap* m, const void* base, long long rows, int D) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, 16};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  decode_cta<D, NT, ROPE>(&kmap, &vmap, a, blockIdx.x, blockIdx.y, blockIdx.z, smem_raw);
 }
 
 template <int D, int NT, bool ROPE>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
-  using GE = Geo<D>;
   const int smem = Smem<D>::TOTAL + 1024;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static bool done[64] = {false};
+  cudaError_t e = set_smem_once(decode_mma_kernel<D, NT, ROPE>, smem, done);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_mma_kernel<D, NT, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
   CUtensorMap km, vm;
   const long long rows = (long long)a.num_blocks * a.Hkv * 16;
   if (!make_pool_map(&km, a.k_pool, rows, D) || !make_pool_map(&vm, a.v_pool, rows, D))

@@ -9,9 +9,11 @@
 // the library holds kNoAllocScratchBytes for it until the process exits.
 //
 // The array is shared by every call on a device and keeps the last call's
-// contents.  Nothing in it needs to start at zero: each split writes its
-// partial before the merge reads it.  Calls whose work overlaps on the GPU
-// (two streams, or concurrent host threads) race on the array; serialize them.
+// contents.  Only the split-completion counters at its start must be zero when
+// a call begins, so each call clears them on its stream first; partial results
+// are always written before they are read.  Calls whose work overlaps on the
+// GPU (two streams, or concurrent host threads) race on the array; serialize
+// them.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -61,6 +63,13 @@ minipic_status minipic_attn_decode_noalloc(minipic_dtype dtype, int32_t num_q_he
   void* scratch = nullptr;
   const minipic_status st = scratch_address(&scratch);
   if (st != MINIPIC_OK) return st;
+  // the split-completion counters (the first batch * kv-heads words, padded to
+  // 256 bytes) must start at zero; clear them rather than trust the last call
+  if (batch->batch > 0 && kv->num_kv_heads > 0) {
+    const size_t cnt = (((size_t)batch->batch * kv->num_kv_heads * sizeof(int)) + 255) / 256 * 256;
+    if (cnt <= kNoAllocScratchBytes && cudaMemsetAsync(scratch, 0, cnt, (cudaStream_t)stream) != cudaSuccess)
+      return MINIPIC_ERR_CUDA;
+  }
   return minipic_attn_decode(dtype, num_q_heads, kv, rope, batch, scale, scratch, kNoAllocScratchBytes, stream);
 }
 

@@ -21,6 +21,7 @@ struct DecodeArgs {
   float* lse;                // [B][Hq] or null
   float* part_o;             // [B][Hq][n_split][D] (unnormalised), null when n_split == 1
   float* part_ml;            // [B][Hq][n_split][2] (max, sum) in log2 units
+  int* counters;             // [B][Hkv] finished splits (zero between calls), null when n_split == 1
   int batch, Hq, Hkv, G, D, BS, num_blocks, max_blocks;
   int split_blocks;          // blocks per split
   int n_split;               // splits per (request, kv head)
@@ -66,5 +67,14 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, bool bf16, bool rotate, cuda
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool rotate, cudaStream_t s);
 cudaError_t launch_decode_merge(const DecodeArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, bool rotate, cudaStream_t s);
+// One grid of prefill tiles followed by decode splits (both with rotation).
+cudaError_t launch_mixed(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s);
+
+// Byte layout of the decode workspace: one completion counter per (request,
+// kv head) first, then partial outputs and partial (max, sum) pairs.
+struct DecodeWs {
+  size_t o_bytes, ml_bytes, cnt_bytes, total;
+};
+DecodeWs decode_ws_layout(int batch, int Hq, int Hkv, int D, int n_split);
 
 }  // namespace minipic

@@ -1,0 +1,81 @@
+"""Mixed continuous batch (span prefills + decodes in ONE launch) against the
+CPU oracle, and against the standalone prefill and decode calls."""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_util import compare, compare_lse, i32, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from position_independent_kv_paged_gb300 import _build
+    _build.build()
+    import position_independent_kv_paged_gb300 as mp
+    mp.load()
+    return torch, mp, torch.device("cuda:0")
+
+
+def run_mixed(env, w):
+    torch, mp, dev = env
+    p, d = w.prefill, w.decode
+    kpool, vpool = to_dev(w.kv.k_pool, "bf16", torch, dev), to_dev(w.kv.v_pool, "bf16", torch, dev)
+    rope = mp.rope_table(w.max_pos, w.d, w.rope_base, device=dev)
+    pre = dict(q=to_dev(p.q, "bf16", torch, dev), cu_q_lens=i32(p.cu_q_lens, torch, dev),
+               q_pos=i32(p.q_pos, torch, dev), block_tables=i32(p.block_tables, torch, dev),
+               block_starts=i32(p.block_starts, torch, dev), kv_lens=i32(p.kv_lens, torch, dev),
+               max_q_len=int(np.diff(p.cu_q_lens).max()),
+               lse=torch.full((int(p.cu_q_lens[-1]), w.Hq), float("nan"), device=dev))
+    dec = dict(q=to_dev(d.q, "bf16", torch, dev), block_tables=i32(d.block_tables, torch, dev),
+               block_starts=i32(d.block_starts, torch, dev), seq_lens=i32(d.seq_lens, torch, dev),
+               q_pos=i32(d.q_pos, torch, dev), lse=torch.full((d.batch, w.Hq), float("nan"), device=dev))
+    po, pl, do, dl = mp.attn_mixed(pre, dec, kpool, vpool, rope)
+    torch.cuda.synchronize()
+    return (po.float().cpu().numpy(), pl.cpu().numpy(), do.float().cpu().numpy(), dl.cpu().numpy(),
+            (pre, dec, kpool, vpool, rope))
+
+
+def test_mixed_scaled_matches_oracle(env):
+    w = W.mixed_batch(5, n_prefill=3, chunk=300, n_decode=6, min_ctx=1, max_ctx=5000)
+    po, pl, do, dl, _ = run_mixed(env, w)
+    rp, rpl = oracle.prefill(w)
+    rd, rdl = oracle.decode(w)
+    compare(po, rp, "bf16", "mixed prefill part")
+    compare_lse(pl, rpl, "bf16", "mixed prefill part")
+    compare(do, rd, "bf16", "mixed decode part")
+    compare_lse(dl, rdl, "bf16", "mixed decode part")
+    assert env[1].device_error() == 0
+
+
+def test_mixed_equals_separate_calls(env):
+    torch, mp, dev = env
+    w = W.mixed_batch(6, n_prefill=2, chunk=200, n_decode=5, min_ctx=100, max_ctx=3000, Hq=16, Hkv=2)
+    po, pl, do, dl, (pre, dec, kpool, vpool, rope) = run_mixed(env, w)
+    so, _ = mp.attn_prefill(pre["q"], pre["cu_q_lens"], pre["q_pos"], kpool, vpool, pre["block_tables"],
+                            pre["block_starts"], pre["kv_lens"], rope, max_q_len=pre["max_q_len"])
+    sd, _ = mp.attn_decode(dec["q"], kpool, vpool, dec["block_tables"], dec["block_starts"], dec["seq_lens"],
+                           dec["q_pos"], rope)
+    torch.cuda.synchronize()
+    assert np.array_equal(so.float().cpu().numpy(), po)
+    assert np.array_equal(sd.float().cpu().numpy(), do)
+
+
+def test_full_size_mixed_sampled(env):
+    w = W.config(4)
+    po, pl, do, dl, _ = run_mixed(env, w)
+    rp, rpl = oracle.prefill(w, requests=[0, 15])
+    rd, rdl = oracle.decode(w, requests=[0, 77, 127])
+    p = w.prefill
+    rows = np.concatenate([np.arange(p.cu_q_lens[r], p.cu_q_lens[r + 1]) for r in (0, 15)])
+    compare(po[rows], rp[rows], "bf16", "mixed full prefill")
+    compare(do[[0, 77, 127]], rd[[0, 77, 127]], "bf16", "mixed full decode")
+    compare_lse(dl[[0, 77, 127]], rdl[[0, 77, 127]], "bf16", "mixed full decode")
+    assert np.all(np.isfinite(po)) and np.all(np.isfinite(do))
+    assert env[1].device_error() == 0
