@@ -318,19 +318,26 @@ def run_minipic(args):
     case = DecodeCase(w, dev, torch, mp)
     nbytes = case.nbytes
 
+    clk = Clocks(local).__enter__()  # sampling every 200 ms from before the warm-up to the end of the timed steps
     for _ in range(max(3, args.warmup)):
         case.step()
     torch.cuda.synchronize()
     if mp.device_error() != 0:
         raise RuntimeError("device error during warm-up")
+    # keep the GPU under the same load (untimed) so that the sampler sees it at steady state
+    t_hold = time.perf_counter()
+    while time.perf_counter() - t_hold < 0.6:
+        for _ in range(20):
+            case.step()
+        torch.cuda.synchronize()
 
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        t_wall = time.perf_counter()
-        ms = timed(torch, stream, flush, case.step, args.steps)
-        t_wall = time.perf_counter() - t_wall
+    t_wall = time.perf_counter()
+    ms = timed(torch, stream, flush, case.step, args.steps)
+    t_wall = time.perf_counter() - t_wall
+    clk.__exit__(None, None, None)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -429,6 +436,39 @@ def run_minipic(args):
         del cp, wp
         torch.cuda.empty_cache()
 
+        # mixed continuous batch: span prefills + decodes in ONE launch, against the parts run alone
+        wm = W.mixed_batch(seed=rank)
+        cmp_ = PrefillCase(wm, dev, torch, mp)
+        cmd = DecodeCase(wm, dev, torch, mp)
+        pre = dict(q=cmp_.q, cu_q_lens=cmp_.cu, q_pos=cmp_.qp, block_tables=cmp_.bt, block_starts=cmp_.st,
+                   kv_lens=cmp_.kvl, max_q_len=cmp_.max_q, out=cmp_.out, lse=cmp_.lse)
+        dec = dict(q=cmd.q, block_tables=cmd.bt, block_starts=cmd.st, seq_lens=cmd.sl, q_pos=cmd.qp,
+                   out=cmd.out, lse=cmd.lse)
+        cmd.kpool, cmd.vpool = cmp_.kpool, cmp_.vpool  # one pool shared by both parts
+
+        def mixed_step():
+            mp.attn_mixed(pre, dec, cmp_.kpool, cmp_.vpool, cmp_.rope, workspace=cmd.ws)
+
+        for fn in (mixed_step, cmp_.step, cmd.step):
+            for _ in range(3):
+                fn()
+        t_mix = timed(torch, stream, flush, mixed_step, args.steps)
+        t_pre = timed(torch, stream, flush, cmp_.step, args.steps)
+        t_dec = timed(torch, stream, flush, cmd.step, args.steps)
+        t_mix, t_pre, t_dec = (sum(x) / len(x) for x in (t_mix, t_pre, t_dec))
+        t_roof = max(cmd.nbytes / (pk["hbm"] * 1e9), cmp_.flops / (pk["bf16"] * 1e12)) * 1e3
+        extras["mixed"] = {"workload": f"{wm.name}: {wm.notes}", "ms_per_step": t_mix,
+                           "decode_kv_bytes": cmd.nbytes, "prefill_flops": cmp_.flops,
+                           "decode_GB_s_equiv": cmd.nbytes / (t_mix * 1e-3) / 1e9,
+                           "prefill_TFLOP_s_equiv": cmp_.flops / (t_mix * 1e-3) / 1e12,
+                           "roofline_ms": t_roof, "combined_frac": t_roof / t_mix,
+                           "separate_ms": {"prefill": t_pre, "decode": t_dec, "sum": t_pre + t_dec},
+                           "launches_per_step": 1}
+        if mp.device_error() != 0:
+            raise RuntimeError("device error in mixed")
+        del cmp_, cmd, wm
+        torch.cuda.empty_cache()
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -436,16 +476,18 @@ def run_minipic(args):
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": dict(workload_desc(w), parallelism=f"replicas{world}" if world > 1 else "single",
                            l2=f"flushed before every step by writing {L2_FLUSH_BYTES >> 20} MiB",
+                           clocks_sampled="nvidia-smi every 200 ms from warm-up through the timed steps, "
+                                          "with 0.6 s of untimed identical decode load before them",
                            logical_kv_bytes=nbytes, unique_kv_bytes=unique_kv_bytes(w)),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                          "frac": achieved / pk["hbm"],
                          "traffic": kernel_traffic("decode_mma.cu", "rag_decode"),
                          "peak_source": pk["src"],
-                         "kernel": "decode call (split kernel + log-sum-exp merge kernel)",
+                         "kernel": "decode_mma_kernel (split-KV with the cross-split merge in-kernel)",
                          "bytes": "logical K+V bytes gathered per request (sum_r L_r * Hkv * d * 2 * 2)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "wall_s_timed": t_wall,
         }

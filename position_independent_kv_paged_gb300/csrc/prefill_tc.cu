@@ -1,33 +1,33 @@
-// Prefill kernel wrapper and launcher (the CTA body is in prefill_body.cuh).
-#include "prefill_body.cuh"
+// Prefill kernel wrapper and launcher (the CTA body is in prefill2_body.cuh).
+#include "prefill2_body.cuh"
 #include "tmap.cuh"
 
 namespace minipic {
 namespace {
 
-using namespace prefill_impl;
+using namespace prefill2_impl;
 
 template <int D, bool ROPE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                      const PrefillLaunch L) {
+                      const PrefillLaunch2 L) {
   extern __shared__ uint8_t smem_raw[];
-  // heaviest (latest) query tiles first
-  prefill_cta<D, ROPE>(&kmap, &vmap, L, gridDim.x - 1 - blockIdx.x, gridDim.x, blockIdx.y, blockIdx.z, smem_raw);
+  // heaviest (latest) query-tile pairs first
+  prefill2_cta<D, ROPE>(&kmap, &vmap, L, gridDim.x - 1 - blockIdx.x, gridDim.x, blockIdx.y, blockIdx.z, smem_raw);
 }
 
 template <int D, bool ROPE>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
-  const int smem = PG<D>::TOTAL + 1024;
+  const int smem = PG2<D>::TOTAL + 1024;
   static bool done[64] = {false};
   cudaError_t e = set_smem_once(prefill_tc_kernel<D, ROPE>, smem, done);
   if (e != cudaSuccess) return e;
   CUtensorMap km, vm;
   const long long rows = (long long)a.num_blocks * a.Hkv * 16;
   if (!make_pool_map(&km, a.k_pool, rows, D) || !make_pool_map(&vm, a.v_pool, rows, D)) return cudaErrorInvalidValue;
-  PrefillLaunch L{a, 128 / a.G};
-  const int n_qt = (a.max_q_len + L.tq - 1) / L.tq;
-  dim3 grid(n_qt, a.Hkv, a.batch);
+  PrefillLaunch2 L{a, 128 / a.G};
+  const int n_pairs = (a.max_q_len + 2 * L.tq - 1) / (2 * L.tq);
+  dim3 grid(n_pairs, a.Hkv, a.batch);
   prefill_tc_kernel<D, ROPE><<<grid, kThreads, smem, s>>>(km, vm, L);
   return cudaGetLastError();
 }
