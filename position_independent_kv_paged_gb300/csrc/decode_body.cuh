@@ -122,25 +122,26 @@ __device__ __forceinline__ uint32_t w_of(const U4& v, int k) {
 }
 
 // Shared-memory plan of one CTA (offsets from a 1024-byte aligned base).
-template <int D>
+template <int D, int NW = kWarps, int NS = kStages>
 struct Smem {
-  static constexpr int STAGES = kWarps * kStages * Geo<D>::STAGE;  // K|V tiles
+  static constexpr int STAGES = NW * NS * Geo<D>::STAGE;  // K|V tiles
   static constexpr int ROWB = 4 * D;                               // one cos|sin table row
   static constexpr int ROWS = STAGES;                              // [warp][stage] table rows
-  static constexpr int META = ROWS + kWarps * kStages * ROWB;      // [split block][phys, start]
+  static constexpr int META = ROWS + NW * NS * ROWB;      // [split block][phys, start]
   static constexpr int kMaxSplit = 512;                            // split_blocks cap (planner)
   static constexpr int BARS = META + kMaxSplit * 8;
-  static constexpr int TOTAL = BARS + kWarps * kStages * 8;
+  static constexpr int TOTAL = BARS + NW * NS * 8;
 };
 
-// One decode CTA: (split, kv head hk, request r).  Threads beyond the 4 working
-// warps (a mixed launch runs 5-warp CTAs) only take part in the CTA barriers.
-template <int D, int NT, bool ROPE>
+// One decode CTA: (split, kv head hk, request r) with NW working warps of NS
+// stages each.  Threads beyond the working warps (a mixed launch shares the CTA
+// shape of the prefill kernel) only take part in the CTA barriers.
+template <int D, int NT, bool ROPE, int NW = kWarps, int NS = kStages>
 __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p,
                                            const DecodeArgs& a, const int split, const int hk, const int r,
                                            uint8_t* smem_raw) {
   using GE = Geo<D>;
-  using SM = Smem<D>;
+  using SM = Smem<D, NW, NS>;
   const CUtensorMap& kmap = *kmap_p;
   const CUtensorMap& vmap = *vmap_p;
   const uint32_t sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -151,7 +152,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g8 = lane >> 2, tig = lane & 3;
   const int G = a.G;
-  const bool worker = warp < kWarps;
+  const bool worker = warp < NW;
   const int mb = a.max_blocks;
 
   int L = a.seq_lens[r];
@@ -166,7 +167,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   const int b_begin = split * a.split_blocks;
   const int b_end = min(nblk, b_begin + a.split_blocks);
   const int span = b_end - b_begin;
-  const int nmine = (worker && span > warp) ? (span - warp + kWarps - 1) / kWarps : 0;
+  const int nmine = (worker && span > warp) ? (span - warp + NW - 1) / NW : 0;
 
   // block ids and start positions of the whole split, staged once
   {
@@ -179,7 +180,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   }
   if (worker && lane == 0) {
 #pragma unroll
-    for (int st = 0; st < kStages; ++st) ptx::mbar_init(bar_base + (warp * kStages + st) * 8, 1);
+    for (int st = 0; st < NS; ++st) ptx::mbar_init(bar_base + (warp * NS + st) * 8, 1);
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
   }
@@ -256,10 +257,10 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   // lane 0: issue the k-th block of this warp into its stage: K and V tiles by
   // TMA, plus the table row |t - start| the block's query rotation needs
   auto issue = [&](int k) {
-    const int i = warp + kWarps * k;
-    const int stg = k % kStages;
-    const uint32_t bar = bar_base + (warp * kStages + stg) * 8;
-    const uint32_t kdst = sbase + (warp * kStages + stg) * GE::STAGE;
+    const int i = warp + NW * k;
+    const int stg = k % NS;
+    const uint32_t bar = bar_base + (warp * NS + stg) * 8;
+    const uint32_t kdst = sbase + (warp * NS + stg) * GE::STAGE;
     const int phys = meta[2 * i];
     if (phys < 0 || phys >= a.num_blocks) {
       ptx::mbar_arrive(bar);  // nothing to load; the consumer masks the block
@@ -280,24 +281,24 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
       ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
     }
     if (row_ok)
-      ptx::bulk_load(sbase + SM::ROWS + (warp * kStages + stg) * SM::ROWB, a.cos_sin + (size_t)ad * D, SM::ROWB,
+      ptx::bulk_load(sbase + SM::ROWS + (warp * NS + stg) * SM::ROWB, a.cos_sin + (size_t)ad * D, SM::ROWB,
                      bar);
   };
   if (lane == 0) {
-    const int pre = nmine < kStages ? nmine : kStages;
+    const int pre = nmine < NS ? nmine : NS;
     for (int k = 0; k < pre; ++k) issue(k);
   }
 
   bool timed_out = false;
   int k_stop = nmine;
   for (int k = 0; k < nmine; ++k) {
-    const int i = warp + kWarps * k;
+    const int i = warp + NW * k;
     const int b = b_begin + i;
-    const int stg = k % kStages;
-    const uint32_t bar = bar_base + (warp * kStages + stg) * 8;
-    const uint32_t kbase = sbase + (warp * kStages + stg) * GE::STAGE;
+    const int stg = k % NS;
+    const uint32_t bar = bar_base + (warp * NS + stg) * 8;
+    const uint32_t kbase = sbase + (warp * NS + stg) * GE::STAGE;
     const uint32_t vbase = kbase + GE::TILE;
-    const uint32_t rowb = sbase + SM::ROWS + (warp * kStages + stg) * SM::ROWB;
+    const uint32_t rowb = sbase + SM::ROWS + (warp * NS + stg) * SM::ROWB;
 
     const int phys = meta[2 * i];
     const bool ok = phys >= 0 && phys < a.num_blocks;
@@ -320,7 +321,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
     }
 
     // wait for this block's tiles (bounded)
-    const bool arrived = ptx::mbar_wait(bar, (uint32_t)((k / kStages) & 1));
+    const bool arrived = ptx::mbar_wait(bar, (uint32_t)((k / NS) & 1));
     if (!__all_sync(0xffffffffu, arrived)) {
       if (lane == 0) atomicOr(a.err, kErrTimeout);
       timed_out = true;
@@ -452,23 +453,23 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
     }
 
     __syncwarp();
-    if (lane == 0 && k + kStages < nmine) issue(k + kStages);
+    if (lane == 0 && k + NS < nmine) issue(k + NS);
   }
 
   if (timed_out) {
-    // blocks k_stop .. k_stop + kStages - 1 were issued and not consumed
+    // blocks k_stop .. k_stop + NS - 1 were issued and not consumed
     if (lane == 0) {
-      const int last = min(nmine, k_stop + kStages);
+      const int last = min(nmine, k_stop + NS);
       for (int k2 = k_stop; k2 < last; ++k2) {
-        const int stg = k2 % kStages;
-        ptx::mbar_wait(bar_base + (warp * kStages + stg) * 8, (uint32_t)((k2 / kStages) & 1), 100000000ull);
+        const int stg = k2 % NS;
+        ptx::mbar_wait(bar_base + (warp * NS + stg) * 8, (uint32_t)((k2 / NS) & 1), 100000000ull);
       }
     }
   }
 
   // per-warp state -> this warp's own stage region: m[16], l[16], O[16][D + 4]
   constexpr int OST = D + 4;  // padded row stride (conflict-free stores)
-  float* wm = reinterpret_cast<float*>(sgen + warp * kStages * GE::STAGE);
+  float* wm = reinterpret_cast<float*>(sgen + warp * NS * GE::STAGE);
   float* wl = wm + 16;
   float* wo = wm + 32;
 #pragma unroll
@@ -510,12 +511,12 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
     const int head = idx / D, dim = idx - head * D;
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-      M = fmaxf(M, reinterpret_cast<const float*>(sgen + w * kStages * GE::STAGE)[head]);
+    for (int w = 0; w < NW; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(sgen + w * NS * GE::STAGE)[head]);
     float Ls = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float* base = reinterpret_cast<const float*>(sgen + w * kStages * GE::STAGE);
+    for (int w = 0; w < NW; ++w) {
+      const float* base = reinterpret_cast<const float*>(sgen + w * NS * GE::STAGE);
       const float mw = base[head];
       const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
       Ls = fmaf(base[16 + head], f, Ls);

@@ -384,7 +384,7 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
         break;
       }
       const int* m = meta + 16 * s;
-      const uint32_t kb = sbase + G_::OFF_K + s * G_::TILE;
+      uint8_t* sk = sg + G_::OFF_K + s * G_::TILE;
 #pragma unroll
       for (int bb = 0; bb < 2; ++bb) {
         const int blk = rw + 4 * bb;
@@ -392,9 +392,11 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
         const int start = m[blk];
         uint64_t ac[4], as[4];
         if (ROPE && (flag & 2)) {
-          const uint32_t rb = sbase + G_::OFF_RS + (s * 8 + blk) * G_::ROWB;
-          const U4 c0 = ptx::lds128(rb + 32 * fg), c1 = ptx::lds128(rb + 32 * fg + 16);
-          const U4 s0 = ptx::lds128(rb + 2 * D + 32 * fg), s1 = ptx::lds128(rb + 2 * D + 32 * fg + 16);
+          const uint8_t* rb = sg + G_::OFF_RS + (s * 8 + blk) * G_::ROWB;
+          const U4 c0 = *reinterpret_cast<const U4*>(rb + 32 * fg);
+          const U4 c1 = *reinterpret_cast<const U4*>(rb + 32 * fg + 16);
+          const U4 s0 = *reinterpret_cast<const U4*>(rb + 2 * D + 32 * fg);
+          const U4 s1 = *reinterpret_cast<const U4*>(rb + 2 * D + 32 * fg + 16);
           ac[0] = ((uint64_t)c0.y << 32) | c0.x; ac[1] = ((uint64_t)c0.w << 32) | c0.z;
           ac[2] = ((uint64_t)c1.y << 32) | c1.x; ac[3] = ((uint64_t)c1.w << 32) | c1.z;
           as[0] = ((uint64_t)s0.y << 32) | s0.x; as[1] = ((uint64_t)s0.w << 32) | s0.z;
@@ -417,12 +419,13 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
             c2[e] = ptx::sub2(ptx::mul2(ac[e], rsc[u][e]), ptx::mul2(as[e], rss[u][e]));
             s2[e] = ptx::fma2(as[e], rsc[u][e], ptx::mul2(ac[e], rss[u][e]));
           }
-          const uint32_t ax = kb + swz(key, fg);
-          const uint32_t ay = (D == 128) ? ax + BN * 128 : kb + swz(key, fg + 4);
-          U4 x = ptx::lds128(ax), y = ptx::lds128(ay);
+          // plain shared-memory accesses (not volatile asm) so that independent keys overlap
+          U4* px = reinterpret_cast<U4*>(sk + swz(key, fg));
+          U4* py = reinterpret_cast<U4*>(sk + ((D == 128) ? BN * 128 + swz(key, fg) : swz(key, fg + 4)));
+          U4 x = *px, y = *py;
           rot_pack(x, y, c2, s2);
-          sts128(ax, x);
-          sts128(ay, y);
+          *px = x;
+          *py = y;
         }
         bits = __reduce_or_sync(0xffffffffu, bits);
         if (lane == 0) mask16[(t & 3) * 8 + blk] = (uint16_t)bits;
@@ -465,13 +468,19 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
       float mx = -CUDART_INF_F;
       if (full) {
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          uint32_t v[32];
-          umma::tmem_ld32(t_s + part * 32, v);
+        float pm[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pm[k] = -CUDART_INF_F;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32], u[32];
+          umma::tmem_ld32(t_s + half * 64, v);
+          umma::tmem_ld32(t_s + half * 64 + 32, u);
           umma::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+          for (int j = 0; j < 32; ++j)
+            pm[j & 7] = fmaxf(pm[j & 7], fmaxf(__uint_as_float(v[j]), __uint_as_float(u[j])));
         }
+        mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       } else {
 #pragma unroll 1
         for (int part = 0; part < 4; ++part) {
@@ -513,24 +522,29 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
       const uint64_t mref2 = ptx::f2(mref, mref);
       // pass 2: P = 2^(s - mref), row sum, bf16 pairs over the S columns
       uint64_t lsum2 = ptx::f2(0.f, 0.f);
+      uint64_t ls[4] = {lsum2, lsum2, lsum2, lsum2};
       if (full) {
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          uint32_t v[32];
-          umma::tmem_ld32(t_s + part * 32, v);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[64];
+          umma::tmem_ld32(t_s + half * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+          umma::tmem_ld32(t_s + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
           umma::tmem_wait_ld();
-          uint32_t w[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint64_t d2 = ptx::sub2(ptx::f2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), mref2);
-            float dl, dh;
-            asm("mov.b64 {%0, %1}, %2;" : "=f"(dl), "=f"(dh) : "l"(d2));
-            const float p0 = ex2(dl), p1 = ex2(dh);
-            const uint64_t p2 = ptx::f2(p0, p1);
-            asm("add.rn.f32x2 %0, %0, %1;" : "+l"(lsum2) : "l"(p2));
-            w[j] = ptx::pack_bf16(p0, p1);
+          for (int q = 0; q < 2; ++q) {
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const uint64_t d2 =
+                  ptx::sub2(ptx::f2(__uint_as_float(v[32 * q + 2 * j]), __uint_as_float(v[32 * q + 2 * j + 1])), mref2);
+              float dl, dh;
+              asm("mov.b64 {%0, %1}, %2;" : "=f"(dl), "=f"(dh) : "l"(d2));
+              const uint64_t p2 = ptx::f2(ex2(dl), ex2(dh));
+              ls[j & 3] = ptx::add2(ls[j & 3], p2);
+              w[j] = ptx::f2_to_bf2(p2);
+            }
+            umma::tmem_st16(t_s + (2 * half + q) * 16, w);
           }
-          umma::tmem_st16(t_s + part * 16, w);
         }
       } else {
 #pragma unroll 1
@@ -554,6 +568,7 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
           umma::tmem_st16(t_s + part * 16, w);
         }
       }
+      lsum2 = ptx::add2(lsum2, ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3])));
       float sl, sh;
       asm("mov.b64 {%0, %1}, %2;" : "=f"(sl), "=f"(sh) : "l"(lsum2));
       l_run += sl + sh;

@@ -63,8 +63,12 @@ def test_mixed_equals_separate_calls(env):
     sd, _ = mp.attn_decode(dec["q"], kpool, vpool, dec["block_tables"], dec["block_starts"], dec["seq_lens"],
                            dec["q_pos"], rope)
     torch.cuda.synchronize()
+    # the prefill tiles run the same CTA body as the standalone kernel: identical bits
     assert np.array_equal(so.float().cpu().numpy(), po)
-    assert np.array_equal(sd.float().cpu().numpy(), do)
+    # decode CTAs in the mixed grid spread a split over 12 warps instead of 4, which
+    # groups the per-warp partial sums differently: equal up to rounding
+    diff = np.abs(sd.float().cpu().numpy() - do)
+    assert diff.max() <= 4e-3 and diff.mean() <= 2e-4
 
 
 def test_full_size_mixed_sampled(env):
