@@ -12,10 +12,12 @@
 // TQ = 128 / G consecutive tokens x the G query heads of kv head hk.  Roles:
 //   warps 0-3   softmax of query tile 0 (thread = TMEM lane = query row)
 //   warps 4-7   softmax of query tile 1
-//   warps 8-11  query preparation, then rotation of every staged key tile
-//   warp 12     TMA producer (K~ tiles + block-start cos/sin rows, V tiles)
-//   warp 13     TMEM allocation and tcgen05 MMA issue
-// K and V are double buffered.  Per 128-key tile t the MMA warp issues
+//   warps 8-13  query preparation, then rotation of every staged key tile
+//   warp 14     TMA producer (K~ tiles + block-start cos/sin rows, V tiles)
+//   warp 15     TMEM allocation and tcgen05 MMA issue
+// A key tile is NB blocks (16 NB keys); K~ has NSK stages and V NSV stages, so
+// a stage freed by the products of tile t is refilled while tiles t+1..t+NSK-1
+// are in flight.  Per key tile t the MMA warp issues
 //   S0 = Q0 K_t^T, S1 = Q1 K_t^T, then O0 += P0 V_t, S0' = Q0 K_{t+1}^T,
 //   O1 += P1 V_t, S1' = Q1 K_{t+1}^T ...
 // so that each softmax warpgroup works on its tile while the tensor core runs
@@ -35,46 +37,54 @@ namespace prefill2_impl {
 using ptx::U4;
 
 constexpr int kSoftThreads = 256;                 // two softmax warpgroups
-constexpr int kRotBase = 256;                     // first thread of the rotation warpgroup
-constexpr int kTmaWarp = 12, kMmaWarp = 13;
-constexpr int kThreads = 14 * 32;
-constexpr int BN = 128;
+constexpr int kRotBase = 256;                     // first thread of the six rotation warps
+constexpr int kRotThreads = 192;
+constexpr int kTmaWarp = 14, kMmaWarp = 15;
+constexpr int kThreads = 16 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.f;
 
-// barriers
-enum {
-  kBarQ = 0,        // rotation warpgroup -> MMA: both query tiles in shared memory
-  kBarKFull = 1,    // [2] TMA -> rotation: K~ stage and its start rows landed
-  kBarKRot = 3,     // [2] rotation -> MMA: K stage rotated
-  kBarKFree = 5,    // [2] MMA -> TMA: K stage consumed
-  kBarVFull = 7,    // [2] TMA -> MMA
-  kBarVFree = 9,    // [2] MMA -> TMA
-  kBarS = 11,       // [2] MMA -> softmax i: S_i ready
-  kBarP = 13,       // [2] softmax i -> MMA: P_i in TMEM
-  kBarODone = 15,   // MMA -> softmax: last products finished
-  kBarMask = 16,    // [4] rotation -> softmax: key-valid bits of tile t (index t & 3)
-  kNumBars = 20
-};
+constexpr int kMaskRing = 8;  // key-valid masks of tiles t & 7
 
-template <int D>
+// Shared memory, barriers and TMEM plan of one CTA.
+// Default tile plan: 96-key tiles, four K~ stages, two V stages (about 222 KB
+// of shared memory for d = 128).
+constexpr int kNB = 6, kNSK = 4, kNSV = 2;
+
+template <int D, int NB = kNB, int NSK = kNSK, int NSV = kNSV>
 struct PG2 {
+  // a mask slot is rewritten for tile t + kMaskRing once K~ stage of tile t + kMaskRing - NSK
+  // is free, i.e. both softmax groups are past tile t + kMaskRing - NSK - 1 >= t
+  static_assert(NB % 2 == 0 && NSK >= NSV && NSV >= 2 && kMaskRing > NSK && (8 * NB) % 16 == 0, "tile plan");
+  static constexpr int BN = 16 * NB;                   // keys per tile
   static constexpr int HALVES = D / 64;
-  static constexpr int TILE = HALVES * BN * 128;      // one Q, K or V tile
-  static constexpr int ROWB = 4 * D;                  // one cos|sin table row
-  static constexpr int OFF_Q = 0;                     // [2] query tiles
-  static constexpr int OFF_K = OFF_Q + 2 * TILE;      // [2] K stages
-  static constexpr int OFF_V = OFF_K + 2 * TILE;      // [2] V stages
-  static constexpr int OFF_RS = OFF_V + 2 * TILE;     // [2 stages][8] block-start rows
-  static constexpr int OFF_META = OFF_RS + 16 * ROWB; // [2 stages] int start[8], int flag[8]
-  static constexpr int OFF_MASK = OFF_META + 2 * 64;  // [4 tiles][8] uint16 key-valid bits per block
-  static constexpr int OFF_BAR = OFF_MASK + 4 * 16;
-  static constexpr int OFF_TSLOT = OFF_BAR + kNumBars * 8;
+  static constexpr int QTILE = HALVES * 128 * 128;     // one 128-row query tile
+  static constexpr int KTILE = HALVES * BN * 128;      // one K or V tile
+  static constexpr int ROWB = 4 * D;                   // one cos|sin table row
+  static constexpr int OFF_Q = 0;                      // [2] query tiles
+  static constexpr int OFF_K = OFF_Q + 2 * QTILE;      // [NSK] K stages
+  static constexpr int OFF_V = OFF_K + NSK * KTILE;    // [NSV] V stages
+  static constexpr int OFF_RS = OFF_V + NSV * KTILE;   // [NSK][NB] block-start rows
+  static constexpr int OFF_META = OFF_RS + NSK * NB * ROWB;  // [NSK] int start[NB], flag[NB], vblock[NB]
+  static constexpr int OFF_MASK = OFF_META + NSK * 3 * NB * 4;  // [ring][NB] uint16 key-valid bits
+  // barriers
+  static constexpr int B_Q = 0, B_KFULL = 1, B_KROT = B_KFULL + NSK, B_KFREE = B_KROT + NSK;
+  static constexpr int B_VFULL = B_KFREE + NSK, B_VFREE = B_VFULL + NSV, B_S = B_VFREE + NSV, B_P = B_S + 2;
+  static constexpr int B_ODONE = B_P + 2, B_MASK = B_ODONE + 1, NBARS = B_MASK + kMaskRing;
+  static constexpr int OFF_BAR = (OFF_MASK + kMaskRing * NB * 2 + 15) / 16 * 16;
+  static constexpr int OFF_TSLOT = OFF_BAR + NBARS * 8;
   static constexpr int TOTAL = OFF_TSLOT + 16;
-  static constexpr int NFG = D / 16;                  // rotation work split: frequency groups of 8
-  static constexpr int SPT = 16 * NFG / 32;           // slots per rotation thread
-  static constexpr uint32_t TCOLS = 512;              // S0 [0,128) S1 [128,256) O0 [256,..) O1 [384,..)
+  // rotation split: thread = (frequency group of 8, slot pair, block group)
+  static constexpr int NFG = D / 16;
+  static constexpr int BG = kRotThreads / (NFG * 8);   // block groups (3 for d 128, 6 for d 64)
+  static constexpr int BPG = NB / BG;                  // blocks per group
+  static_assert(BG * NFG * 8 == kRotThreads && NB % BG == 0, "rotation split");
+  // S_i at [128 i, 128 i + BN), P_i (bf16 pairs) over its first BN / 2 columns,
+  // O_i at [256 + 128 i, 256 + 128 i + D)
+  static constexpr uint32_t TCOLS = 512;
+  static_assert(BN <= 128 && BN % 32 == 0, "TMEM plan");
+  static_assert(BN <= 128 && TOTAL + 1024 <= 232448, "tile plan");
 };
 
 struct PrefillLaunch2 {
@@ -111,18 +121,24 @@ __device__ __forceinline__ void rot_pack(U4& x, U4& y, const uint64_t (&c2)[4], 
   y = U4{yw[0], yw[1], yw[2], yw[3]};
 }
 
-template <int D, bool ROPE>
+// MC: the CTA is one of a 2-CTA cluster whose other CTA (query-tile pair
+// peer_pair of the same request and kv head) reads the same K~/V tiles; each
+// CTA fetches the boxes of half the blocks of a tile and multicasts them to
+// both, and a stage is refilled only once both CTAs have released it.
+// vmap_p is the block view of the V pool (make_pool_block_map).
+template <int D, bool ROPE, bool MC = false, int NB = kNB, int NSK = kNSK, int NSV = kNSV>
 __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p,
-                                             const PrefillLaunch2& L, const int pair, const int n_pairs,
-                                             const int hk, const int r, uint8_t* smem_raw) {
-  using G_ = PG2<D>;
+                                             const PrefillLaunch2& L, const int pair, const int peer_pair,
+                                             const int n_pairs, const int hk, const int r, uint8_t* smem_raw) {
+  using G_ = PG2<D, NB, NSK, NSV>;
+  constexpr int BN = G_::BN;
   const PrefillArgs& a = L.a;
   const CUtensorMap& kmap = *kmap_p;
   const CUtensorMap& vmap = *vmap_p;
   const uint32_t sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
   uint8_t* sg = smem_raw + (sbase - ptx::smem_addr(smem_raw));
-  int* meta = reinterpret_cast<int*>(sg + G_::OFF_META);  // [stage][16]: start[8], flag[8]
-  uint16_t* mask16 = reinterpret_cast<uint16_t*>(sg + G_::OFF_MASK);
+  int* meta = reinterpret_cast<int*>(sg + G_::OFF_META);  // [stage][3 NB]: start, flag, V block id
+  uint16_t* mask16 = reinterpret_cast<uint16_t*>(sg + G_::OFF_MASK);  // [ring][NB] key-valid bits
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sg + G_::OFF_TSLOT);
   const uint32_t bar0 = sbase + G_::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -133,31 +149,41 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
   const int ql = a.cu_q_lens[r + 1] - q0;
   const int tok0 = 2 * pair * TQ;  // first token of query tile 0
   if (tid == 0 && pair == n_pairs - 1 && ql > n_pairs * 2 * TQ) atomicOr(a.err, kErrSeqLen);
-  if (ql <= 0 || tok0 >= ql) return;
+  auto has_rows = [&](int pr) { return pr >= 0 && ql > 0 && 2 * pr * TQ < ql; };
+  if (!has_rows(pair) && (!MC || !has_rows(peer_pair))) return;  // the same in both CTAs of a cluster
   int kvl = a.kv_lens[r];
   if (kvl < ql || kvl > mb * 16) {
     if (tid == 0 && pair == 0) atomicOr(a.err, kErrSeqLen);
     kvl = min(kvl, mb * 16);
   }
   const int nblk = (kvl + 15) >> 4;
-  const int ntok_all = min(2 * TQ, ql - tok0);
-  const int lim_last = kvl - ql + tok0 + ntok_all - 1;  // largest key any row of the pair sees
-  const int n_kt = lim_last >= 0 ? lim_last / BN + 1 : 0;
+  auto tiles_of = [&](int pr) {  // key tiles the rows of query-tile pair pr reach
+    if (!has_rows(pr)) return 0;
+    const int t0 = 2 * pr * TQ;
+    const int lim_last = kvl - ql + t0 + min(2 * TQ, ql - t0) - 1;
+    return lim_last >= 0 ? lim_last / BN + 1 : 0;
+  };
+  const int n_kt = tiles_of(pair);                                  // tiles this CTA computes on
+  const int n_ld = MC ? max(n_kt, tiles_of(peer_pair)) : n_kt;      // tiles this CTA helps load
 
   // ------------------------------------------------------------ setup
   if (tid == 0) {
-    ptx::mbar_init(bar(kBarQ), 128);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(bar(kBarKFull + s), 1);
-      ptx::mbar_init(bar(kBarKRot + s), 128);
-      ptx::mbar_init(bar(kBarKFree + s), 1);
-      ptx::mbar_init(bar(kBarVFull + s), 1);
-      ptx::mbar_init(bar(kBarVFree + s), 1);
-      ptx::mbar_init(bar(kBarS + s), 1);
-      ptx::mbar_init(bar(kBarP + s), 128);
+    ptx::mbar_init(bar(G_::B_Q), kRotThreads);
+    for (int s = 0; s < NSK; ++s) {
+      ptx::mbar_init(bar(G_::B_KFULL + s), 1);
+      ptx::mbar_init(bar(G_::B_KROT + s), kRotThreads);
+      ptx::mbar_init(bar(G_::B_KFREE + s), MC ? 2 : 1);
     }
-    ptx::mbar_init(bar(kBarODone), 1);
-    for (int k = 0; k < 4; ++k) ptx::mbar_init(bar(kBarMask + k), 128);
+    for (int s = 0; s < NSV; ++s) {
+      ptx::mbar_init(bar(G_::B_VFULL + s), 1);
+      ptx::mbar_init(bar(G_::B_VFREE + s), MC ? 2 : 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(G_::B_S + i), 1);
+      ptx::mbar_init(bar(G_::B_P + i), kSoftThreads / 2);
+    }
+    ptx::mbar_init(bar(G_::B_ODONE), 1);
+    for (int k = 0; k < kMaskRing; ++k) ptx::mbar_init(bar(G_::B_MASK + k), kRotThreads);
     ptx::fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -165,147 +191,206 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
     umma::tmem_relinquish();
   }
   // zero K and V stages once so that never-loaded blocks hold finite values
-  for (int i = tid; i < 4 * G_::TILE / 16; i += kThreads)
+  for (int i = tid; i < (NSK + NSV) * G_::KTILE / 16; i += kThreads)
     reinterpret_cast<uint4*>(sg + G_::OFF_K)[i] = make_uint4(0u, 0u, 0u, 0u);
   ptx::fence_proxy_async_smem();
   umma::fence_before_sync();
   __syncthreads();
+  if constexpr (MC) ptx::cluster_sync();  // the peer's barriers exist before anything is multicast
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
+  const uint32_t crank = MC ? ptx::cluster_rank() : 0u;
+  constexpr uint16_t kBoth = 3;
 
   if (warp == kTmaWarp) {
     // ======================================================== TMA producer
-    if (lane == 0 && n_kt > 0) {
+    // Step u loads K~ tile u (once the products of tile u - NSK freed its stage)
+    // and V tile u - LAG (once tile u - LAG - NSV freed its stage): K~ runs LAG
+    // tiles ahead of V so that rotation has time to work on it.  The whole warp
+    // issues a tile's copies together (lane -> block lane % NB, half lane / NB;
+    // the lanes after those fetch the block-start cos/sin rows): one thread
+    // issuing every copy in turn cannot keep up with the tensor core.
+    constexpr int LAG = NSK - NSV;
+    constexpr unsigned FULL = 0xffffffffu;
+    static_assert(NB * G_::HALVES + NB <= 32, "one lane per copy");
+    if (n_ld > 0) {
       const int* bt = a.block_tables + (size_t)r * mb;
       const int* bs = a.block_starts + (size_t)r * mb;
-      int nph[8], nst[8], vph[8][2];
-      auto load_meta = [&](int t) {
-#pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
-          const int b = 8 * t + blk;
-          nph[blk] = b < nblk ? __ldg(bt + b) : -1;
-          nst[blk] = b < nblk ? __ldg(bs + b) : 0;
-        }
+      const int blk = lane % NB, hh = lane / NB;
+      const bool mine = !MC || (uint32_t)(blk & 1) == crank;  // with MC: blocks of this CTA's parity
+      int my_ph = -1, my_st = 0;  // lanes < NB: block NB u + lane of the next K~ tile
+      auto fetch = [&](int t) {
+        const int b = NB * t + lane;
+        const bool in = lane < NB && b < nblk;
+        my_ph = in ? __ldg(bt + b) : -1;
+        my_st = in ? __ldg(bs + b) : 0;
       };
       bool ok = true;
-      load_meta(0);
-      for (int t = 0; t < n_kt && ok; ++t) {
-        const int s = t & 1;
-        if (t >= 2 && !ptx::mbar_wait(bar(kBarKFree + s), ((t >> 1) - 1) & 1)) { ok = false; break; }
-        int* m = meta + 16 * s;
-        int nvalid = 0, nrows = 0;
-#pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
-          const int b = 8 * t + blk;
+      fetch(0);
+      for (int u = 0; u < n_ld + LAG; ++u) {
+        if (u < n_ld) {
+          const int s = u % NSK;
+          bool w = true;
+          if (lane == 0 && u >= NSK) w = ptx::mbar_wait(bar(G_::B_KFREE + s), ((u / NSK) - 1) & 1);
+          if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
           int flag = 0;
-          if (b < nblk) {
-            if (nph[blk] >= 0 && nph[blk] < a.num_blocks) flag |= 1;
-            else atomicOr(a.err, kErrBlockId);
-            if (!ROPE || (nst[blk] >= 0 && nst[blk] < a.max_pos)) flag |= 2;
+          if (lane < NB && NB * u + lane < nblk) {
+            if (my_ph >= 0 && my_ph < a.num_blocks) flag |= 1;
+            else if (crank == 0) atomicOr(a.err, kErrBlockId);
+            if (!ROPE || (my_st >= 0 && my_st < a.max_pos)) flag |= 2;
           }
-          m[blk] = nst[blk];
-          m[8 + blk] = flag;
-          vph[blk][s] = (flag & 1) ? nph[blk] : -1;
-          nvalid += flag & 1;
-          nrows += (ROPE && (flag & 3) == 3) ? 1 : 0;
+          int* m = meta + 3 * NB * s;
+          if (lane < NB) {
+            m[lane] = my_st;
+            m[NB + lane] = flag;
+            m[2 * NB + lane] = (flag & 1) ? my_ph : -1;
+          }
+          const unsigned kv = __ballot_sync(FULL, flag & 1);
+          const unsigned rw = __ballot_sync(FULL, ROPE && (flag & 3) == 3);
+          const int ph_l = __shfl_sync(FULL, my_ph, blk);
+          const int st_l = __shfl_sync(FULL, my_st, blk);
+          __syncwarp();
+          if (lane == 0)
+            ptx::mbar_arrive_expect_tx(bar(G_::B_KFULL + s), __popc(kv) * G_::HALVES * 2048 + __popc(rw) * G_::ROWB);
+          __syncwarp();
+          if (lane < NB * G_::HALVES) {
+            if (mine && ((kv >> blk) & 1u)) {
+              const uint32_t dst = sbase + G_::OFF_K + s * G_::KTILE + hh * (BN * 128) + blk * 2048;
+              if constexpr (MC)
+                ptx::tma_load_2d_mc(dst, &kmap, 64 * hh, (ph_l * a.Hkv + hk) * 16, bar(G_::B_KFULL + s), kBoth);
+              else
+                ptx::tma_load_2d(dst, &kmap, 64 * hh, (ph_l * a.Hkv + hk) * 16, bar(G_::B_KFULL + s));
+            }
+          } else if (ROPE && lane < NB * G_::HALVES + NB) {
+            if (mine && ((rw >> blk) & 1u)) {
+              const uint32_t dst = sbase + G_::OFF_RS + (s * NB + blk) * G_::ROWB;
+              if constexpr (MC)
+                ptx::bulk_load_mc(dst, a.cos_sin + (size_t)st_l * D, G_::ROWB, bar(G_::B_KFULL + s), kBoth);
+              else
+                ptx::bulk_load(dst, a.cos_sin + (size_t)st_l * D, G_::ROWB, bar(G_::B_KFULL + s));
+            }
+          }
+          if (u + 1 < n_ld) fetch(u + 1);
         }
-        ptx::mbar_arrive_expect_tx(bar(kBarKFull + s), nvalid * G_::HALVES * 2048 + nrows * G_::ROWB);
-#pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
-          if (vph[blk][s] < 0) continue;
-          const int y = (vph[blk][s] * a.Hkv + hk) * 16;
-          for (int hh = 0; hh < G_::HALVES; ++hh)
-            ptx::tma_load_2d(sbase + G_::OFF_K + s * G_::TILE + hh * (BN * 128) + blk * 2048, &kmap, 64 * hh, y,
-                             bar(kBarKFull + s));
-          if (ROPE && (m[8 + blk] & 3) == 3)
-            ptx::bulk_load(sbase + G_::OFF_RS + (s * 8 + blk) * G_::ROWB, a.cos_sin + (size_t)nst[blk] * D,
-                           G_::ROWB, bar(kBarKFull + s));
-        }
-        if (t + 1 < n_kt) load_meta(t + 1);
-        if (t >= 2 && !ptx::mbar_wait(bar(kBarVFree + s), ((t >> 1) - 1) & 1)) { ok = false; break; }
-        int vvalid = 0;
-#pragma unroll
-        for (int blk = 0; blk < 8; ++blk) vvalid += vph[blk][s] >= 0 ? 1 : 0;
-        ptx::mbar_arrive_expect_tx(bar(kBarVFull + s), vvalid * G_::HALVES * 2048);
-#pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
-          if (vph[blk][s] < 0) continue;
-          const int y = (vph[blk][s] * a.Hkv + hk) * 16;
-          for (int hh = 0; hh < G_::HALVES; ++hh)
-            ptx::tma_load_2d(sbase + G_::OFF_V + s * G_::TILE + hh * (BN * 128) + blk * 2048, &vmap, 64 * hh, y,
-                             bar(kBarVFull + s));
+        const int tv = u - LAG;
+        if (tv >= 0) {
+          const int sv = tv % NSV;
+          bool w = true;
+          if (lane == 0 && tv >= NSV) w = ptx::mbar_wait(bar(G_::B_VFREE + sv), ((tv / NSV) - 1) & 1);
+          if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
+          // the meta of tile tv is rewritten only for tile tv + NSK > u
+          const int ph = meta[3 * NB * (tv % NSK) + 2 * NB + blk];
+          const unsigned vv = __ballot_sync(FULL, lane < NB && ph >= 0);
+          if (lane == 0) ptx::mbar_arrive_expect_tx(bar(G_::B_VFULL + sv), __popc(vv) * G_::HALVES * 2048);
+          __syncwarp();
+          if (lane < NB && ph >= 0 && mine) {  // one box per block: [half][16 rows][64]
+            const uint32_t dst = sbase + G_::OFF_V + sv * G_::KTILE + blk * (G_::HALVES * 2048);
+            if constexpr (MC)
+              ptx::tma_load_3d_mc(dst, &vmap, 0, (ph * a.Hkv + hk) * 16, 0, bar(G_::B_VFULL + sv), kBoth);
+            else
+              ptx::tma_load_3d(dst, &vmap, 0, (ph * a.Hkv + hk) * 16, 0, bar(G_::B_VFULL + sv));
+          }
         }
       }
-      if (!ok) atomicOr(a.err, kErrTimeout);
+      if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ======================================================== MMA issue
-    if (lane == 0 && n_kt > 0) {
+    if (lane == 0 && n_ld > 0) {
+      // release a K~ / V stage: to both CTAs with MC, and there only while some
+      // later tile of the cluster still refills it (so no arrival outlives a peer)
+      auto free_k = [&](int u) {
+        if (!MC) umma::commit(bar(G_::B_KFREE + u % NSK));
+        else if (u + NSK < n_ld) umma::commit_mc(bar(G_::B_KFREE + u % NSK), kBoth);
+      };
+      auto free_v = [&](int u) {
+        if (!MC) umma::commit(bar(G_::B_VFREE + u % NSV));
+        else if (u + NSV < n_ld) umma::commit_mc(bar(G_::B_VFREE + u % NSV), kBoth);
+      };
       const uint32_t id_qk = ROPE ? umma::idesc_f16_f32(128, BN, false, false)
                                   : umma::idesc_bf16_f32(128, BN, false, false);
       const uint32_t id_pv = umma::idesc_bf16_f32(128, D, false, true);
       auto qk = [&](int i, int t) {
-        const uint32_t kb = sbase + G_::OFF_K + (t & 1) * G_::TILE;
-        const uint32_t qb = sbase + G_::OFF_Q + i * G_::TILE;
+        const uint32_t kb = sbase + G_::OFF_K + (t % NSK) * G_::KTILE;
+        const uint32_t qb = sbase + G_::OFF_Q + i * G_::QTILE;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * (BN * 128) + (ks & 3) * 32;
-          umma::mma_ss(tmem + 128 * i, umma::smem_desc_sw128(qb + off, 16, 1024),
-                       umma::smem_desc_sw128(kb + off, 16, 1024), id_qk, ks > 0);
+          const uint32_t cb = (ks & 3) * 32;
+          umma::mma_ss(tmem + 128 * i, umma::smem_desc_sw128(qb + (ks >> 2) * (128 * 128) + cb, 16, 1024),
+                       umma::smem_desc_sw128(kb + (ks >> 2) * (BN * 128) + cb, 16, 1024), id_qk, ks > 0);
         }
-        umma::commit(bar(kBarS + i));
+        umma::commit(bar(G_::B_S + i));
       };
-      auto pv = [&](int i, int t) {
-        const uint32_t vb = sbase + G_::OFF_V + (t & 1) * G_::TILE;
+      auto pv = [&](int i, int t) {  // V stage: [block][half][16 keys][64]
+        const uint32_t vb = sbase + G_::OFF_V + (t % NSV) * G_::KTILE;
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
+        for (int ks = 0; ks < NB; ++ks)
           umma::mma_ts(tmem + 256 + 128 * i, tmem + 128 * i + 8 * ks,
-                       umma::smem_desc_sw128(vb + ks * 2048, BN * 128, 1024), id_pv, (t > 0 || ks > 0) ? 1u : 0u);
+                       umma::smem_desc_sw128(vb + ks * (G_::HALVES * 2048), 2048, 1024), id_pv,
+                       (t > 0 || ks > 0) ? 1u : 0u);
       };
-      bool ok = ptx::mbar_wait(bar(kBarQ), 0) && ptx::mbar_wait(bar(kBarKRot), 0);
-      if (ok) {
-        umma::fence_after_sync();
-        qk(0, 0);
-        qk(1, 0);
-        umma::commit(bar(kBarKFree + 0));
+      bool ok = true;
+      if (n_kt > 0) {
+        ok = ptx::mbar_wait(bar(G_::B_Q), 0) && ptx::mbar_wait(bar(G_::B_KROT), 0);
+        if (ok) {
+          umma::fence_after_sync();
+          qk(0, 0);
+          qk(1, 0);
+          free_k(0);
+        }
+        for (int t = 0; t < n_kt && ok; ++t) {
+          const int sv = t % NSV, sk1 = (t + 1) % NSK;
+          const bool more = t + 1 < n_kt;
+          if (!ptx::mbar_wait(bar(G_::B_P + 0), t & 1) || !ptx::mbar_wait(bar(G_::B_VFULL + sv), (t / NSV) & 1)) {
+            ok = false;
+            break;
+          }
+          umma::fence_after_sync();
+          pv(0, t);
+          if (more) {
+            if (!ptx::mbar_wait(bar(G_::B_KROT + sk1), ((t + 1) / NSK) & 1)) { ok = false; break; }
+            umma::fence_after_sync();
+            qk(0, t + 1);
+          }
+          if (!ptx::mbar_wait(bar(G_::B_P + 1), t & 1)) { ok = false; break; }
+          umma::fence_after_sync();
+          pv(1, t);
+          free_v(t);
+          if (more) {
+            qk(1, t + 1);
+            free_k(t + 1);
+          }
+        }
+        umma::commit(bar(G_::B_ODONE));
       }
-      for (int t = 0; t < n_kt && ok; ++t) {
-        const int s = t & 1;
-        const bool more = t + 1 < n_kt;
-        if (!ptx::mbar_wait(bar(kBarP + 0), t & 1) || !ptx::mbar_wait(bar(kBarVFull + s), (t >> 1) & 1)) {
+      // tiles loaded only for the cluster peer: wait for them to land, then release
+      for (int u = n_kt; MC && ok && u < n_ld; ++u) {
+        if (!ptx::mbar_wait(bar(G_::B_KFULL + u % NSK), (u / NSK) & 1) ||
+            !ptx::mbar_wait(bar(G_::B_VFULL + u % NSV), (u / NSV) & 1)) {
           ok = false;
           break;
         }
-        umma::fence_after_sync();
-        pv(0, t);
-        if (more) {
-          if (!ptx::mbar_wait(bar(kBarKRot + ((t + 1) & 1)), ((t + 1) >> 1) & 1)) { ok = false; break; }
-          umma::fence_after_sync();
-          qk(0, t + 1);
+        if (u + NSK < n_ld) {
+          ptx::mbar_arrive_remote(bar(G_::B_KFREE + u % NSK), 0);
+          ptx::mbar_arrive_remote(bar(G_::B_KFREE + u % NSK), 1);
         }
-        if (!ptx::mbar_wait(bar(kBarP + 1), t & 1)) { ok = false; break; }
-        umma::fence_after_sync();
-        pv(1, t);
-        umma::commit(bar(kBarVFree + s));
-        if (more) {
-          qk(1, t + 1);
-          umma::commit(bar(kBarKFree + ((t + 1) & 1)));
+        if (u + NSV < n_ld) {
+          ptx::mbar_arrive_remote(bar(G_::B_VFREE + u % NSV), 0);
+          ptx::mbar_arrive_remote(bar(G_::B_VFREE + u % NSV), 1);
         }
       }
-      umma::commit(bar(kBarODone));
       if (!ok) atomicOr(a.err, kErrTimeout);
     }
     __syncwarp();
   } else if (tid >= kRotBase) {
     // ======================================================== query preparation + key rotation
-    const int rt = tid - kRotBase;  // 0..127
+    const int rt = tid - kRotBase;  // 0..255
     const int rw = rt >> 5;         // warp within the group
     const float qs = a.scale * kLog2e;
-    // ---- query tiles: row rt of tile 0 and of tile 1
 #pragma unroll 1
-    for (int i = 0; i < 2; ++i) {
-      const int row = rt;
+    for (int qr = rt; qr < 256; qr += kRotThreads) {  // ---- query tiles: row qr % 128 of tile qr / 128
+      const int i = qr >> 7, row = qr & 127;
       const int rtok = row / G, rh = row - rtok * G;
       const int tq = tok0 + i * TQ + rtok;
       const bool row_ok = rtok < TQ && tq < ql;
@@ -357,86 +442,98 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
       }
 #pragma unroll
       for (int c = 0; c < D / 8; ++c)
-        sts128(sbase + G_::OFF_Q + i * G_::TILE + (c >> 3) * (BN * 128) + swz(row, c & 7), qc[c]);
+        sts128(sbase + G_::OFF_Q + i * G_::QTILE + (c >> 3) * (128 * 128) + swz(row, c & 7), qc[c]);
     }
     ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(bar(kBarQ));
+    ptx::mbar_arrive(bar(G_::B_Q));
 
-    // ---- key rotation: thread -> (frequency group fg, slot group sgp, blocks rw and rw + 4)
+    // ---- key rotation: thread -> (frequency group fg, slot pair sp, block group
+    // bg): slots 2 sp and 2 sp + 1 of blocks BPG bg .. BPG bg + BPG - 1, so the
+    // slots' own cos/sin(slot theta_f), f = 8 fg .. 8 fg + 7, stay in registers
     const int fg = rt % G_::NFG;
-    const int sgp = (rt / G_::NFG) % (32 / G_::NFG);
-    uint64_t rsc[G_::SPT][4], rss[G_::SPT][4];  // cos/sin(slot theta_f), f = 8 fg .. 8 fg + 7
+    const int sp = (rt / G_::NFG) & 7;
+    const int bg = rt / (G_::NFG * 8);
+    uint64_t rsc[2][4], rss[2][4];
+    if constexpr (ROPE) {
 #pragma unroll
-    for (int u = 0; u < (ROPE ? G_::SPT : 0); ++u) {
-      const float* tr = a.cos_sin + (size_t)min(sgp * G_::SPT + u, a.max_pos - 1) * D;
+      for (int k = 0; k < 2; ++k) {
+        const float* tr = a.cos_sin + (size_t)min(2 * sp + k, a.max_pos - 1) * D;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 c = __ldg(reinterpret_cast<const float2*>(tr + 8 * fg + 2 * e));
-        const float2 sn = __ldg(reinterpret_cast<const float2*>(tr + D / 2 + 8 * fg + 2 * e));
-        rsc[u][e] = ptx::f2(c.x, c.y);
-        rss[u][e] = ptx::f2(sn.x, sn.y);
+        for (int e = 0; e < 4; ++e) {
+          const float2 c = __ldg(reinterpret_cast<const float2*>(tr + 8 * fg + 2 * e));
+          const float2 sn = __ldg(reinterpret_cast<const float2*>(tr + D / 2 + 8 * fg + 2 * e));
+          rsc[k][e] = ptx::f2(c.x, c.y);
+          rss[k][e] = ptx::f2(sn.x, sn.y);
+        }
       }
     }
     for (int t = 0; t < n_kt; ++t) {
-      const int s = t & 1;
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarKFull + s), (t >> 1) & 1))) {
+      const int s = t % NSK;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar(G_::B_KFULL + s), (t / NSK) & 1))) {
         if (lane == 0) atomicOr(a.err, kErrTimeout);
         break;
       }
-      const int* m = meta + 16 * s;
-      uint8_t* sk = sg + G_::OFF_K + s * G_::TILE;
+      const int* m = meta + 3 * NB * s;
+      uint8_t* sk = sg + G_::OFF_K + s * G_::KTILE;
+      if constexpr (ROPE) {
+        // loads for every key first (stage and start rows are always addressable),
+        // stores only for valid keys: no branch between keys, so their loads overlap
 #pragma unroll
-      for (int bb = 0; bb < 2; ++bb) {
-        const int blk = rw + 4 * bb;
-        const int flag = m[8 + blk];
-        const int start = m[blk];
-        uint64_t ac[4], as[4];
-        if (ROPE && (flag & 2)) {
-          const uint8_t* rb = sg + G_::OFF_RS + (s * 8 + blk) * G_::ROWB;
+        for (int b = 0; b < G_::BPG; ++b) {
+          const int blk = bg * G_::BPG + b;
+          const int flag = m[NB + blk];
+          const int start = m[blk];
+          const uint8_t* rb = sg + G_::OFF_RS + (s * NB + blk) * G_::ROWB;
           const U4 c0 = *reinterpret_cast<const U4*>(rb + 32 * fg);
           const U4 c1 = *reinterpret_cast<const U4*>(rb + 32 * fg + 16);
           const U4 s0 = *reinterpret_cast<const U4*>(rb + 2 * D + 32 * fg);
           const U4 s1 = *reinterpret_cast<const U4*>(rb + 2 * D + 32 * fg + 16);
-          ac[0] = ((uint64_t)c0.y << 32) | c0.x; ac[1] = ((uint64_t)c0.w << 32) | c0.z;
-          ac[2] = ((uint64_t)c1.y << 32) | c1.x; ac[3] = ((uint64_t)c1.w << 32) | c1.z;
-          as[0] = ((uint64_t)s0.y << 32) | s0.x; as[1] = ((uint64_t)s0.w << 32) | s0.z;
-          as[2] = ((uint64_t)s1.y << 32) | s1.x; as[3] = ((uint64_t)s1.w << 32) | s1.z;
-        } else {
+          const uint64_t ac[4] = {((uint64_t)c0.y << 32) | c0.x, ((uint64_t)c0.w << 32) | c0.z,
+                                  ((uint64_t)c1.y << 32) | c1.x, ((uint64_t)c1.w << 32) | c1.z};
+          const uint64_t as[4] = {((uint64_t)s0.y << 32) | s0.x, ((uint64_t)s0.w << 32) | s0.z,
+                                  ((uint64_t)s1.y << 32) | s1.x, ((uint64_t)s1.w << 32) | s1.z};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) ac[e] = as[e] = 0ull;
-        }
-        uint32_t bits = 0;
+          for (int k = 0; k < 2; ++k) {
+            const int slot = 2 * sp + k;
+            const int key = blk * 16 + slot;
+            const bool v = (flag & 3) == 3 && t * BN + key < kvl && start + slot < a.max_pos;
+            U4* px = reinterpret_cast<U4*>(sk + swz(key, fg));
+            U4* py = reinterpret_cast<U4*>(sk + ((D == 128) ? BN * 128 + swz(key, fg) : swz(key, fg + 4)));
+            U4 x = *px, y = *py;
+            uint64_t c2[4], s2[4];  // cos/sin((start + slot) theta) by angle addition
 #pragma unroll
-        for (int u = 0; u < G_::SPT; ++u) {
-          const int slot = sgp * G_::SPT + u;
-          const int key = blk * 16 + slot;
-          const bool v = (flag & 3) == 3 && t * BN + key < kvl && (!ROPE || start + slot < a.max_pos);
-          bits |= v ? (1u << slot) : 0u;
-          if (!ROPE || !v) continue;
-          uint64_t c2[4], s2[4];  // cos/sin((start + slot) theta) by angle addition
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            c2[e] = ptx::sub2(ptx::mul2(ac[e], rsc[u][e]), ptx::mul2(as[e], rss[u][e]));
-            s2[e] = ptx::fma2(as[e], rsc[u][e], ptx::mul2(ac[e], rss[u][e]));
+            for (int e = 0; e < 4; ++e) {
+              c2[e] = ptx::sub2(ptx::mul2(ac[e], rsc[k][e]), ptx::mul2(as[e], rss[k][e]));
+              s2[e] = ptx::fma2(as[e], rsc[k][e], ptx::mul2(ac[e], rss[k][e]));
+            }
+            rot_pack(x, y, c2, s2);
+            if (v) {
+              *px = x;
+              *py = y;
+            }
           }
-          // plain shared-memory accesses (not volatile asm) so that independent keys overlap
-          U4* px = reinterpret_cast<U4*>(sk + swz(key, fg));
-          U4* py = reinterpret_cast<U4*>(sk + ((D == 128) ? BN * 128 + swz(key, fg) : swz(key, fg + 4)));
-          U4 x = *px, y = *py;
-          rot_pack(x, y, c2, s2);
-          *px = x;
-          *py = y;
         }
-        bits = __reduce_or_sync(0xffffffffu, bits);
-        if (lane == 0) mask16[(t & 3) * 8 + blk] = (uint16_t)bits;
+      }
+      // key-valid bits: warp rw covers blocks rw, rw + 6, ...; lane = slot
+#pragma unroll
+      for (int blk = rw; blk < NB; blk += kRotThreads / 32) {
+        const int flag = m[NB + blk];
+        const int start = m[blk];
+        const bool v = lane < 16 && (flag & 3) == 3 && t * BN + blk * 16 + lane < kvl &&
+                       (!ROPE || start + lane < a.max_pos);
+        const uint32_t bits = __ballot_sync(0xffffffffu, v);
+        if (lane == 0) mask16[(t % kMaskRing) * NB + blk] = (uint16_t)bits;
       }
       ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(bar(kBarMask + (t & 3)));
-      ptx::mbar_arrive(bar(kBarKRot + s));
+      ptx::mbar_arrive(bar(G_::B_MASK + t % kMaskRing));
+      ptx::mbar_arrive(bar(G_::B_KROT + s));
     }
   } else {
     // ======================================================== softmax of query tile i
-    const int i = tid >> 7;       // 0 or 1
+    // The row's BN scores are read from TMEM once; the max, the reference
+    // update and P (packed in place over the scores) all come from registers.
+    constexpr int NP = BN / 32;  // 32-key parts of a tile
+    const int i = warp >> 2;      // 0 or 1
     const int row = tid & 127;    // TMEM lane
     const int rtok = row / G, rh = row - rtok * G;
     const int tq = tok0 + i * TQ + rtok;
@@ -449,50 +546,46 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
     float m_run = -CUDART_INF_F, m_use = -CUDART_INF_F, l_run = 0.f;
     bool failed = false;
     for (int t = 0; t < n_kt; ++t) {
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarS + i), t & 1))) {
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar(G_::B_S + i), t & 1))) {
+        failed = true;
+        break;
+      }
+      // the mask of tile t is rewritten for tile t + kMaskRing, which needs this group past tile t + 3
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar(G_::B_MASK + t % kMaskRing), (t / kMaskRing) & 1))) {
         failed = true;
         break;
       }
       umma::fence_after_sync();
-      // the mask of tile t is rewritten only for tile t + 4, after this group finished tile t + 1
-      if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarMask + (t & 3)), (t >> 2) & 1))) {
-        failed = true;
-        break;
+      uint32_t v[BN];
+#pragma unroll
+      for (int part = 0; part < NP; ++part)
+        umma::tmem_ld32(t_s + 32 * part, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * part));
+      const uint16_t* mk = mask16 + (t % kMaskRing) * NB;
+      uint32_t mw[NP];
+      uint32_t mall = 0xffffffffu;
+#pragma unroll
+      for (int w = 0; w < NP; ++w) {
+        mw[w] = (uint32_t)mk[2 * w] | ((uint32_t)mk[2 * w + 1] << 16);
+        mall &= mw[w];
       }
-      const uint16_t* mk = mask16 + (t & 3) * 8;
-      uint32_t mw[4];
-#pragma unroll
-      for (int w = 0; w < 4; ++w) mw[w] = (uint32_t)mk[2 * w] | ((uint32_t)mk[2 * w + 1] << 16);
-      const bool full = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu && t * BN + BN - 1 <= lim_first;
-      // pass 1: row max
-      float mx = -CUDART_INF_F;
+      const bool full = mall == 0xffffffffu && t * BN + BN - 1 <= lim_first;
+      const int kb0 = t * BN;
+      umma::tmem_wait_ld();
+      float mx;
       if (full) {
+        float pm[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-        float pm[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = -CUDART_INF_F;
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32], u[32];
-          umma::tmem_ld32(t_s + half * 64, v);
-          umma::tmem_ld32(t_s + half * 64 + 32, u);
-          umma::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            pm[j & 7] = fmaxf(pm[j & 7], fmaxf(__uint_as_float(v[j]), __uint_as_float(u[j])));
-        }
-        mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        for (int j = 0; j < BN; j += 2)
+          pm[(j >> 1) & 3] = ptx::fmax3(pm[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+        mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
       } else {
-#pragma unroll 1
-        for (int part = 0; part < 4; ++part) {
-          uint32_t v[32];
-          umma::tmem_ld32(t_s + part * 32, v);
-          umma::tmem_wait_ld();
-          const int kb0 = t * BN + part * 32;
+        // invalid keys become -inf in place, so that both passes treat them alike
+        mx = -CUDART_INF_F;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const bool ok = row_ok && ((mw[part] >> j) & 1u) && kb0 + j <= lim;
-            mx = ok ? fmaxf(mx, __uint_as_float(v[j])) : mx;
-          }
+        for (int j = 0; j < BN; ++j) {
+          const bool ok = row_ok && ((mw[j >> 5] >> (j & 31)) & 1u) && kb0 + j <= lim;
+          v[j] = ok ? v[j] : __float_as_uint(-CUDART_INF_F);
+          mx = fmaxf(mx, __uint_as_float(v[j]));
         }
       }
       m_run = fmaxf(m_run, mx);
@@ -502,83 +595,49 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
         l_run *= corr;
         m_use = m_run;
       }
+      // P = 2^(s - mref) as bf16 pairs, written over the scores already consumed
+      // (pair j lands in v[j] after v[2 j], v[2 j + 1] were read), 16 words per store
+      const float mref = m_use == -CUDART_INF_F ? 0.f : m_use;
+      const uint64_t mref2 = ptx::f2(mref, mref);
+      uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+      for (int j = 0; j < BN / 2; ++j) {
+        const uint64_t d2 = ptx::sub2(ptx::f2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), mref2);
+        float dl, dh;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(dl), "=f"(dh) : "l"(d2));
+        const uint64_t p2 = ptx::f2(ex2(dl), ex2(dh));  // 2^-inf = 0 for masked keys
+        ls[j & 3] = ptx::add2(ls[j & 3], p2);
+        v[j] = ptx::f2_to_bf2(p2);
+        if ((j & 15) == 15) umma::tmem_st16(t_s + (j & ~15), *reinterpret_cast<const uint32_t(*)[16]>(v + (j & ~15)));
+      }
+      const uint64_t lsum2 = ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3]));
+      float sl, sh;
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(sl), "=f"(sh) : "l"(lsum2));
+      l_run += sl + sh;
+      // lazy O rescale before P_i releases the next products
       if (t > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
         for (int part = 0; part < D / 32; ++part) {
-          uint32_t v[32];
-          umma::tmem_ld32(t_o + part * 32, v);
+          uint32_t o[32];
+          umma::tmem_ld32(t_o + part * 32, o);
           umma::tmem_wait_ld();
           uint32_t w0[16], w1[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            w0[j] = __float_as_uint(__uint_as_float(v[j]) * corr);
-            w1[j] = __float_as_uint(__uint_as_float(v[16 + j]) * corr);
+            w0[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
+            w1[j] = __float_as_uint(__uint_as_float(o[16 + j]) * corr);
           }
           umma::tmem_st16(t_o + part * 32, w0);
           umma::tmem_st16(t_o + part * 32 + 16, w1);
         }
       }
-      const float mref = m_use == -CUDART_INF_F ? 0.f : m_use;
-      const uint64_t mref2 = ptx::f2(mref, mref);
-      // pass 2: P = 2^(s - mref), row sum, bf16 pairs over the S columns
-      uint64_t lsum2 = ptx::f2(0.f, 0.f);
-      uint64_t ls[4] = {lsum2, lsum2, lsum2, lsum2};
-      if (full) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[64];
-          umma::tmem_ld32(t_s + half * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
-          umma::tmem_ld32(t_s + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-          umma::tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint64_t d2 =
-                  ptx::sub2(ptx::f2(__uint_as_float(v[32 * q + 2 * j]), __uint_as_float(v[32 * q + 2 * j + 1])), mref2);
-              float dl, dh;
-              asm("mov.b64 {%0, %1}, %2;" : "=f"(dl), "=f"(dh) : "l"(d2));
-              const uint64_t p2 = ptx::f2(ex2(dl), ex2(dh));
-              ls[j & 3] = ptx::add2(ls[j & 3], p2);
-              w[j] = ptx::f2_to_bf2(p2);
-            }
-            umma::tmem_st16(t_s + (2 * half + q) * 16, w);
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int part = 0; part < 4; ++part) {
-          uint32_t v[32];
-          umma::tmem_ld32(t_s + part * 32, v);
-          umma::tmem_wait_ld();
-          const int kb0 = t * BN + part * 32;
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int j0 = 2 * j, j1 = 2 * j + 1;
-            const bool ok0 = row_ok && ((mw[part] >> j0) & 1u) && kb0 + j0 <= lim;
-            const bool ok1 = row_ok && ((mw[part] >> j1) & 1u) && kb0 + j1 <= lim;
-            const float p0 = ok0 ? ex2(__uint_as_float(v[j0]) - mref) : 0.f;
-            const float p1 = ok1 ? ex2(__uint_as_float(v[j1]) - mref) : 0.f;
-            const uint64_t p2 = ptx::f2(p0, p1);
-            asm("add.rn.f32x2 %0, %0, %1;" : "+l"(lsum2) : "l"(p2));
-            w[j] = ptx::pack_bf16(p0, p1);
-          }
-          umma::tmem_st16(t_s + part * 16, w);
-        }
-      }
-      lsum2 = ptx::add2(lsum2, ptx::add2(ptx::add2(ls[0], ls[1]), ptx::add2(ls[2], ls[3])));
-      float sl, sh;
-      asm("mov.b64 {%0, %1}, %2;" : "=f"(sl), "=f"(sh) : "l"(lsum2));
-      l_run += sl + sh;
       umma::tmem_wait_st();
       umma::fence_before_sync();
-      ptx::mbar_arrive(bar(kBarP + i));
+      ptx::mbar_arrive(bar(G_::B_P + i));
     }
     // ---- epilogue: O / l -> global (TMEM loads by the whole warp, stores by valid rows)
     bool have = n_kt > 0 && !failed;
-    if (have && !__all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarODone), 0))) {
+    if (have && !__all_sync(0xffffffffu, ptx::mbar_wait(bar(G_::B_ODONE), 0))) {
       have = false;
       failed = true;
     }
@@ -616,6 +675,7 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
   umma::fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) umma::tmem_dealloc(tmem, G_::TCOLS);
+  if constexpr (MC) ptx::cluster_sync();  // no CTA leaves while its peer may still write to it
 }
 
 }  // namespace prefill2_impl

@@ -36,6 +36,21 @@ inline bool make_pool_map(CUtensorMap* m, const void* base, long long rows, int 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same pool as a 3-D view (x = 64 columns, y = row, z = 64-column half) so
+// that one 64 x 16 x (d / 64) box brings a whole 16-row block of one head,
+// landing in shared memory as [half][row][64] (2 KiB per half).
+inline bool make_pool_block_map(CUtensorMap* m, const void* base, long long rows, int D) {
+  auto fn = tmap_encode_fn();
+  if (!fn || rows <= 0) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+  cuuint32_t box[3] = {64, 16, (cuuint32_t)(D / 64)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Set the dynamic shared-memory limit of a kernel once per device.
 template <typename K>
 inline cudaError_t set_smem_once(K kernel, int bytes, bool (&done)[64]) {
