@@ -29,6 +29,25 @@ METRIC = "RoPE-on-load paged attn: decode HBM GB/s (% peak), prefill TFLOP/s (% 
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 
 
+def rank_seed(rank: int) -> int:
+    """Each rank decodes its own synthetic batch (weak scaling): the seed is the rank."""
+    return rank
+
+
+def max_over_ranks(torch, dist, ms_step: float, device) -> float:
+    """The slowest rank's step time (ms); the value itself when running alone."""
+    if dist is None:
+        return ms_step
+    t = torch.tensor([ms_step], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(nbytes_per_rank: int, world: int, ms_step: float) -> float:
+    """Logical bytes all ranks moved in one step / the slowest rank's step time."""
+    return nbytes_per_rank * world / (ms_step * 1e-3) / 1e9
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -313,7 +332,7 @@ def run_minipic(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     # the headline workload: each rank decodes its own batch (weak scaling, no collective)
-    w = W.rag_decode(seed=rank)
+    w = W.rag_decode(seed=rank_seed(rank))
     d = w.decode
     case = DecodeCase(w, dev, torch, mp)
     nbytes = case.nbytes
@@ -341,12 +360,8 @@ def run_minipic(args):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    ms_step = sum(ms) / len(ms)
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = nbytes * world / (ms_step * 1e-3) / 1e9
+    ms_step = max_over_ranks(torch, dist, sum(ms) / len(ms), dev)
+    value = whole_job_gbs(nbytes, world, ms_step)
     achieved = nbytes / (ms_step * 1e-3) / 1e9
 
     extras = {}
