@@ -48,6 +48,45 @@ def whole_job_gbs(nbytes_per_rank: int, world: int, ms_step: float) -> float:
     return nbytes_per_rank * world / (ms_step * 1e-3) / 1e9
 
 
+def append_leg(torch, mp, W, np, dev, stream, flush, pk, rank, steps):
+    """Time minipic_kv_append: GB/s of (read new rows + write pool rows) against HBM."""
+    def one(w, tables, kv_start, n_new):
+        cu = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+        total = int(cu[-1])
+        kp = torch.empty(w.kv.k_pool.shape, dtype=torch.bfloat16, device=dev)
+        vp = torch.empty_like(kp)
+        kn = torch.randn(total, w.Hkv, w.d, device=dev).to(torch.bfloat16)
+        vn = torch.randn_like(kn)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+        cu_d, ks_d, bt_d = i32(cu), i32(kv_start), i32(tables)
+        mx = int(np.max(n_new))
+        step = lambda: mp.kv_append(kn, vn, cu_d, ks_d, bt_d, kp, vp, max_new_len=mx)
+        for _ in range(3):
+            step()
+        ms = statistics.median(timed(torch, stream, flush, step, steps))
+        nbytes = 2 * 2 * total * w.Hkv * w.d * 2  # K and V, read once and written once
+        return ms, nbytes, total
+
+    wp = W.rag_prefill(seed=rank)
+    p = wp.prefill
+    q_lens = np.diff(p.cu_q_lens)
+    ms, nb, tot = one(wp, p.block_tables, p.kv_lens - q_lens, q_lens)
+    del wp
+    wd = W.rag_decode(seed=rank)
+    d = wd.decode
+    # the new token is the request's next key index; the tables get one more column (block 0 stands in
+    # for the block a serving loop would allocate)
+    tables = np.concatenate([d.block_tables, np.zeros((d.batch, 1), dtype=np.int32)], axis=1)
+    ms_d, nb_d, tot_d = one(wd, tables, d.seq_lens, np.ones(d.batch, dtype=np.int64))
+    del wd
+    gbs = nb / (ms * 1e-3) / 1e9
+    return {"workload": f"rag_prefill chunks: {tot} tokens x 8 kv heads x d 128 bf16; "
+                        f"decode: {tot_d} tokens (one per request)",
+            "chunk_ms": ms, "chunk_GB_s": gbs, "chunk_frac_of_hbm": gbs / pk["hbm"], "chunk_bytes": nb,
+            "decode_us": ms_d * 1e3, "decode_bytes": nb_d,
+            "note": "bytes = new K and V rows read + pool rows written; pool and rows resident in HBM"}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -450,6 +489,12 @@ def run_minipic(args):
             raise RuntimeError("device error in prefill")
         del cp, wp
         torch.cuda.empty_cache()
+
+        # cache append of unrotated keys and values: the RAG prefill's own chunks
+        # (8 x 512 tokens) and one decode token per request of the headline batch
+        extras["kv_append"] = append_leg(torch, mp, W, np, dev, stream, flush, pk, rank, args.steps)
+        if mp.device_error() != 0:
+            raise RuntimeError("device error in kv_append")
 
         # mixed continuous batch: span prefills + decodes in ONE launch, against the parts run alone
         wm = W.mixed_batch(seed=rank)

@@ -242,6 +242,48 @@ minipic_status minipic_attn_prefill_prerotated(minipic_dtype dtype, int32_t num_
                                                const minipic_kv_pool* kv, const minipic_prefill_batch* batch,
                                                float scale, minipic_stream_t stream);
 
+/* ------------------------------------------------------------------ cache append
+ * Storing new tokens in the position-free cache (MiniPIC summary, section 2.1:
+ * the cache holds unrotated key vectors k~_j, so a token's key is written
+ * exactly as produced, with no rotation at any position; a block written this
+ * way can later be read at any offset). */
+
+/* Writable view of the pools (same layout as minipic_kv_pool). */
+typedef struct {
+  void* k_pool;           /* [num_blocks][num_kv_heads][block_size][head_dim] */
+  void* v_pool;
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  int32_t block_size;     /* must be 16 */
+  int32_t head_dim;       /* 64 or 128 */
+} minipic_kv_pool_mut;
+
+/* New tokens: token i of request r is row cu_new_lens[r] + i of k_new / v_new
+ * and becomes the request's key index j = kv_start[r] + i, stored in block
+ * block_tables[r][j / 16], slot j % 16, for every kv head. */
+typedef struct {
+  const void* k_new;            /* [total_new][num_kv_heads][head_dim], unrotated keys */
+  const void* v_new;            /* [total_new][num_kv_heads][head_dim] */
+  const int32_t* cu_new_lens;   /* [batch + 1], cu_new_lens[0] = 0 */
+  const int32_t* kv_start;      /* [batch] key index of each request's first new token */
+  const int32_t* block_tables;  /* [batch][max_blocks_per_seq] */
+  int32_t batch;
+  int32_t total_new;            /* cu_new_lens[batch] */
+  int32_t max_new_len;          /* an upper bound of every request's new-token count (grid planning) */
+  int32_t max_blocks_per_seq;
+} minipic_kv_append_batch;
+
+/* Copy the new keys and values into their slots (for a prefill chunk's own
+ * tokens or one decode token per request).  Device memory throughout,
+ * 16-byte aligned rows; dtype f32 or bf16 (the pools' and the new rows' type).
+ * A block id outside [0, num_blocks) sets MINIPIC_DEVERR_BLOCK_ID, a key index
+ * outside the table (or a negative kv_start) sets MINIPIC_DEVERR_SEQ_LEN; such
+ * tokens are skipped, the rest are written.  Every slot must be the target of
+ * at most one token of a call (two tokens mapped to one slot race).
+ * Asynchronous on `stream`. */
+minipic_status minipic_kv_append(minipic_dtype dtype, const minipic_kv_pool_mut* kv,
+                                 const minipic_kv_append_batch* batch, minipic_stream_t stream);
+
 /* Read the device error word (MINIPIC_DEVERR_* bits, 0 if none) of the current
  * device after the work queued on `stream` has finished (this call
  * synchronizes the stream), and reset it to 0 when `clear` is nonzero.

@@ -57,6 +57,13 @@ class _KV(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
+class _Append(ctypes.Structure):
+    _fields_ = [("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("cu_new_lens", ctypes.c_void_p),
+                ("kv_start", ctypes.c_void_p), ("block_tables", ctypes.c_void_p), ("batch", ctypes.c_int32),
+                ("total_new", ctypes.c_int32), ("max_new_len", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32)]
+
+
 class _Rope(ctypes.Structure):
     _fields_ = [("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
@@ -120,6 +127,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         L.minipic_attn_mixed.restype = ctypes.c_int
         L.minipic_attn_mixed.argtypes = [ctypes.c_int, c_i32, ctypes.POINTER(_KV), ctypes.POINTER(_Rope),
                                          ctypes.POINTER(_Prefill), ctypes.POINTER(_Decode), c_f, c_vp, c_sz, c_vp]
+        L.minipic_kv_append.restype = ctypes.c_int
+        L.minipic_kv_append.argtypes = [ctypes.c_int, ctypes.POINTER(_KV), ctypes.POINTER(_Append), c_vp]
         L.minipic_device_error.restype = ctypes.c_int
         L.minipic_device_error.argtypes = [ctypes.POINTER(c_i32), c_i32, c_vp]
         _lib = L
@@ -365,3 +374,31 @@ def device_error(clear: bool = True, stream=None) -> int:
     if st not in (0, 5):
         raise MiniPICError(st, "minipic_device_error")
     return int(flags.value)
+
+
+def kv_append(k_new, v_new, cu_new_lens, kv_start, block_tables, k_pool, v_pool, max_new_len=None,
+              stream=None):
+    """Write new unrotated keys and values into their paged slots, in place:
+    token i of request r (rows cu_new_lens[r] + i of k_new / v_new) becomes key
+    index kv_start[r] + i, block block_tables[r][j // 16], slot j % 16.
+    ``max_new_len`` bounds every request's count (read from cu_new_lens if None,
+    which synchronizes)."""
+    torch = _torch()
+    L = load()
+    kv = _kv(k_pool, v_pool)
+    _need(k_new, "k_new", dtype=k_pool.dtype, ndim=3)
+    _need(v_new, "v_new", dtype=k_pool.dtype, ndim=3)
+    if tuple(k_new.shape) != tuple(v_new.shape) or k_new.shape[1:] != (kv.num_kv_heads, kv.head_dim):
+        raise ValueError("k_new / v_new must be [total_new, num_kv_heads, head_dim]")
+    for name, t in (("cu_new_lens", cu_new_lens), ("kv_start", kv_start)):
+        _need(t, name, dtype=torch.int32, ndim=1)
+    _need(block_tables, "block_tables", dtype=torch.int32, ndim=2)
+    B = kv_start.shape[0]
+    if cu_new_lens.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("cu_new_lens must have batch + 1 entries and block_tables batch rows")
+    if max_new_len is None:
+        max_new_len = int((cu_new_lens[1:] - cu_new_lens[:-1]).max().item()) if B else 0
+    ab = _Append(k_new.data_ptr(), v_new.data_ptr(), cu_new_lens.data_ptr(), kv_start.data_ptr(),
+                 block_tables.data_ptr(), B, k_new.shape[0], int(max_new_len), block_tables.shape[1])
+    _check(L.minipic_kv_append(_dtype_code(k_pool), ctypes.byref(kv), ctypes.byref(ab), _stream(stream)),
+           "minipic_kv_append")

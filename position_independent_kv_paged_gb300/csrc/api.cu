@@ -384,6 +384,44 @@ minipic_status minipic_attn_mixed(minipic_dtype dtype, int32_t num_q_heads, cons
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 
+minipic_status minipic_kv_append(minipic_dtype dtype, const minipic_kv_pool_mut* kv,
+                                 const minipic_kv_append_batch* b, minipic_stream_t stream) {
+  if (dtype != MINIPIC_F32 && dtype != MINIPIC_BF16) return MINIPIC_ERR_INVALID;
+  if (!kv || !b) return MINIPIC_ERR_INVALID;
+  if (kv->num_blocks < 0 || kv->num_kv_heads <= 0 || kv->block_size <= 0 || kv->head_dim <= 0)
+    return MINIPIC_ERR_INVALID;
+  if (b->batch < 0 || b->total_new < 0 || b->max_new_len < 0 || b->max_blocks_per_seq < 0)
+    return MINIPIC_ERR_INVALID;
+  if (kv->head_dim != 64 && kv->head_dim != 128) return MINIPIC_ERR_UNSUPPORTED;
+  if (kv->block_size != 16) return MINIPIC_ERR_UNSUPPORTED;
+  if (b->batch == 0 || b->total_new == 0 || b->max_new_len == 0) return MINIPIC_OK;
+  if (b->batch > 65535 || b->max_blocks_per_seq == 0 || kv->num_blocks == 0) return MINIPIC_ERR_INVALID;
+  if (!b->k_new || !b->v_new || !b->cu_new_lens || !b->kv_start || !b->block_tables || !kv->k_pool ||
+      !kv->v_pool)
+    return MINIPIC_ERR_INVALID;
+  if (!aligned16(b->k_new) || !aligned16(b->v_new) || !aligned16(kv->k_pool) || !aligned16(kv->v_pool))
+    return MINIPIC_ERR_INVALID;
+  int* err = nullptr;
+  if (device_info(&err, nullptr) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  AppendArgs a{};
+  a.k_new = b->k_new;
+  a.v_new = b->v_new;
+  a.cu_new = b->cu_new_lens;
+  a.kv_start = b->kv_start;
+  a.block_tables = b->block_tables;
+  a.k_pool = kv->k_pool;
+  a.v_pool = kv->v_pool;
+  a.batch = b->batch;
+  a.max_new = b->max_new_len;
+  a.max_blocks = b->max_blocks_per_seq;
+  a.num_blocks = kv->num_blocks;
+  a.Hkv = kv->num_kv_heads;
+  a.D = kv->head_dim;
+  a.elem = dtype == MINIPIC_BF16 ? 2 : 4;
+  a.err = err;
+  return launch_kv_append(a, (cudaStream_t)stream) == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
 minipic_status minipic_device_error(int32_t* flags_out, int32_t clear, minipic_stream_t stream) {
   int* err = nullptr;
   if (device_info(&err, nullptr) != cudaSuccess) return MINIPIC_ERR_CUDA;

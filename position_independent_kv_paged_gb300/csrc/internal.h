@@ -70,6 +70,20 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, bool rotate, cudaStream_t s)
 // One grid of prefill tiles followed by decode splits (both with rotation).
 cudaError_t launch_mixed(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s);
 
+// Cache append: token i of request r -> key index kv_start[r] + i.
+struct AppendArgs {
+  const void* k_new;  // [total_new][Hkv][D]
+  const void* v_new;
+  const int32_t* cu_new;      // [batch + 1]
+  const int32_t* kv_start;    // [batch]
+  const int32_t* block_tables;  // [batch][max_blocks]
+  void* k_pool;  // [num_blocks][Hkv][16][D]
+  void* v_pool;
+  int batch, max_new, max_blocks, num_blocks, Hkv, D, elem;
+  int* err;
+};
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t s);
+
 // Byte layout of the decode workspace: one completion counter per (request,
 // kv head) first, then partial outputs and partial (max, sum) pairs.
 struct DecodeWs {

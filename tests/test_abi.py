@@ -100,3 +100,19 @@ def test_workspace_size_is_pure_host(lib):
     n = lib.minipic_attn_decode_workspace_size(8, 64, 8, 128, 8192, 16)
     assert n >= 0
     assert lib.minipic_attn_decode_workspace_size(0, 64, 8, 128, 8192, 16) == 0
+
+
+def test_kv_append_validation(lib):
+    KV, App = mp._KV, mp._Append
+    f = lib.minipic_kv_append
+    kv = KV(None, None, 4, 2, 16, 128)
+    empty = App(None, None, None, None, None, 0, 0, 0, 1)
+    assert f(1, ctypes.byref(kv), ctypes.byref(empty), None) == 0            # nothing to do
+    assert f(7, ctypes.byref(kv), ctypes.byref(empty), None) == 1            # bad dtype
+    assert f(1, None, ctypes.byref(empty), None) == 1                        # no pool
+    assert f(1, ctypes.byref(KV(None, None, 4, 2, 16, 96)), ctypes.byref(empty), None) == 2  # head_dim 96
+    assert f(1, ctypes.byref(KV(None, None, 4, 2, 8, 128)), ctypes.byref(empty), None) == 2  # block size 8
+    bad = App(None, None, None, None, None, -1, 0, 0, 1)
+    assert f(1, ctypes.byref(kv), ctypes.byref(bad), None) == 1              # negative batch
+    nulls = App(None, None, None, None, None, 2, 5, 3, 1)
+    assert f(1, ctypes.byref(kv), ctypes.byref(nulls), None) == 1            # missing pointers

@@ -13,29 +13,7 @@ import workloads as W
 
 
 def _append_case(seed=0, dtype="bf16"):
-    """Four requests holding 5, 16, 31 and 0 keys in distinct random blocks (a
-    request owns the slots it appends into), random block starts, and a ragged
-    append of 20, 1, 17 and 3 new keys that crosses block boundaries."""
-    rng = np.random.default_rng(seed + 100)
-    seq = np.asarray([5, 16, 31, 0], dtype=np.int32)
-    n_new = np.asarray([20, 1, 17, 3], dtype=np.int64)
-    B, Hkv, d, nblk = 4, 2, 64, 20
-    need = int(((seq + n_new + 15) // 16).max())
-    perm = rng.permutation(nblk).astype(np.int32)
-    bt = perm[:B * need].reshape(B, need)
-    st = rng.integers(0, 4096 - 16, size=(B, need)).astype(np.int32)
-    k = W._normal(rng, (nblk, Hkv, 16, d), dtype)
-    v = W._normal(rng, (nblk, Hkv, 16, d), dtype)
-    q = W._normal(rng, (B, 4, d), dtype)
-    dec = W.DecodeBatch(q=q, block_tables=bt, block_starts=st, seq_lens=seq,
-                        q_pos=rng.integers(0, 4096, size=B).astype(np.int32))
-    w = W.Workload("append_case", dtype, 4, Hkv, d, 16, 10000.0, 4096, W.PagedKV(k, v), decode=dec)
-    kv_start = seq.astype(np.int64)
-    cu = np.concatenate([[0], np.cumsum(n_new)])
-    shape = (int(cu[-1]), Hkv, d)
-    k_new = W._normal(rng, shape, dtype)
-    v_new = W._normal(rng, shape, dtype)
-    return w, k_new, v_new, cu, kv_start
+    return W.append_case(seed, dtype)
 
 
 def _slots_written(w, cu, kv_start):

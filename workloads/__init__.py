@@ -425,6 +425,33 @@ def mixed_batch(seed: int = 0, dtype: str = "bf16", n_prefill: int = 16,
 CONFIG_NAMES = ("tiny_decode", "rag_decode", "rag_prefill", "long_decode", "mixed_batch")
 
 
+def append_case(seed: int = 0, dtype: str = "bf16", d: int = 64, Hkv: int = 2,
+                seq_lens: Sequence[int] = (5, 16, 31, 0), n_new: Sequence[int] = (20, 1, 17, 3),
+                pool_blocks: Optional[int] = None):
+    """A cache-append case: requests holding ``seq_lens`` keys in distinct random
+    physical blocks (a request owns the slots it appends into), random block
+    starts, tables wide enough for ``n_new`` more keys, and the new unrotated
+    keys and values.  Returns (workload, k_new, v_new, cu_new, kv_start)."""
+    rng = np.random.default_rng(seed + 100)
+    seq = np.asarray(seq_lens, dtype=np.int32)
+    nn = np.asarray(n_new, dtype=np.int64)
+    B = len(seq)
+    need = int(((seq + nn + BLOCK_SIZE - 1) // BLOCK_SIZE).max()) if B else 1
+    nblk = pool_blocks or B * need + 4
+    perm = rng.permutation(nblk).astype(np.int32)
+    bt = perm[:B * need].reshape(B, need)
+    st = rng.integers(0, 4096 - BLOCK_SIZE, size=(B, need)).astype(np.int32)
+    k = _normal(rng, (nblk, Hkv, BLOCK_SIZE, d), dtype)
+    v = _normal(rng, (nblk, Hkv, BLOCK_SIZE, d), dtype)
+    q = _normal(rng, (B, 2 * Hkv, d), dtype)
+    dec = DecodeBatch(q=q, block_tables=bt, block_starts=st, seq_lens=seq,
+                      q_pos=rng.integers(0, 4096, size=B).astype(np.int32))
+    w = Workload("append_case", dtype, 2 * Hkv, Hkv, d, BLOCK_SIZE, 10000.0, 4096, PagedKV(k, v), decode=dec)
+    cu = np.concatenate([[0], np.cumsum(nn)]).astype(np.int64)
+    shape = (int(cu[-1]), Hkv, d)
+    return w, _normal(rng, shape, dtype), _normal(rng, shape, dtype), cu, seq.astype(np.int64)
+
+
 def config(index: int, seed: int = 0, dtype: Optional[str] = None, **kw) -> Workload:
     """The five workloads by index 0..4 (full sizes unless overridden)."""
     if index == 0:
