@@ -45,3 +45,36 @@ def gather(pool, block_table_row, first: int, count: int, block_size: int = 16):
     if not out:
         return np.zeros((0,) + pool.shape[1:2] + pool.shape[3:], dtype=pool.dtype)
     return np.stack(out)
+
+
+# ---------------------------------------------------------------- host offload
+# MiniPIC summary (gist.science 2606.13126), section 3, item 5: unrotated blocks
+# move between GPU and host with no position to track or adjust.  A block's
+# logical positions live in the requests' block_starts, not in its contents or
+# its physical id, so offload is a plain copy and a block may come back to any
+# free physical id as long as the tables are remapped.
+
+def swap_out(k_pool, v_pool, block_ids):
+    """Host copies [n][Hkv][bs][d] of the listed blocks (K and V)."""
+    ids = np.asarray(block_ids, dtype=np.int64)
+    return np.array(k_pool[ids], copy=True), np.array(v_pool[ids], copy=True)
+
+
+def swap_in(k_pool, v_pool, k_host, v_host, block_ids):
+    """Pools with host block i written to physical block block_ids[i]."""
+    k_out = np.array(k_pool, copy=True)
+    v_out = np.array(v_pool, copy=True)
+    for i, b in enumerate(np.asarray(block_ids, dtype=np.int64)):
+        k_out[b] = k_host[i]
+        v_out[b] = v_host[i]
+    return k_out, v_out
+
+
+def remap_tables(block_tables, old_ids, new_ids):
+    """Tables with every entry old_ids[i] replaced by new_ids[i] (starts unchanged)."""
+    m = {int(o): int(n) for o, n in zip(old_ids, new_ids)}
+    out = np.array(block_tables, copy=True)
+    for idx, b in np.ndenumerate(out):
+        if int(b) in m:
+            out[idx] = m[int(b)]
+    return out

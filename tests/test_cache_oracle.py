@@ -132,3 +132,52 @@ def test_planted_mistakes_are_caught():
     kr = _append_rotated(w, k_new, cu, kv_start)
     got = cache.gather(kr, d.block_tables[2], int(kv_start[2]), 3)
     assert not np.allclose(got, k_new[cu[2]:cu[2] + 3])
+
+
+# ---------------------------------------------------------------- host offload
+
+def _offload_case(dtype="bf16"):
+    """rag-like decode over shared spans; the blocks of request 0 go to the host
+    and come back to fresh physical ids."""
+    w = W.rag_decode(6, dtype, B=4, Hq=8, Hkv=2, d=64, system_tokens=32, n_spans=3, span_tokens=64,
+                     pool_spans=6, tail_tokens=32)
+    d = w.decode
+    n0 = -(-int(d.seq_lens[0]) // 16)
+    old = np.unique(d.block_tables[0, :n0])
+    nb = w.kv.num_blocks
+    new = np.arange(nb, nb + len(old))  # fresh ids past the current pool
+    grow = lambda a: np.concatenate([a, np.zeros((len(old),) + a.shape[1:], dtype=a.dtype)])
+    return w, old, new, grow(w.kv.k_pool), grow(w.kv.v_pool)
+
+
+def test_swap_round_trip_is_identity():
+    w, old, new, kp, vp = _offload_case()
+    kh, vh = cache.swap_out(kp, vp, old)
+    kc, vc = kp.copy(), vp.copy()
+    kc[old] = 0
+    vc[old] = 0
+    k2, v2 = cache.swap_in(kc, vc, kh, vh, old)
+    assert np.array_equal(k2, kp) and np.array_equal(v2, vp)
+
+
+def test_relocated_blocks_need_no_position_fixup():
+    """Blocks swapped out and back in at other physical ids, with the tables
+    remapped and block_starts untouched, give the same attention bit for bit."""
+    w, old, new, kp, vp = _offload_case()
+    ref, ref_lse = oracle.decode(w)
+    kh, vh = cache.swap_out(kp, vp, old)
+    kc, vc = kp.copy(), vp.copy()
+    kc[old] = 0  # the old copies are gone
+    vc[old] = 0
+    k2, v2 = cache.swap_in(kc, vc, kh, vh, new)
+    d = w.decode
+    d2 = W.DecodeBatch(q=d.q, block_tables=cache.remap_tables(d.block_tables, old, new).astype(np.int32),
+                       block_starts=d.block_starts, seq_lens=d.seq_lens, q_pos=d.q_pos)
+    w2 = W.Workload(**{**w.__dict__, "kv": W.PagedKV(k2, v2), "decode": d2})
+    out, lse = oracle.decode(w2)
+    assert np.array_equal(out, ref) and np.array_equal(lse, ref_lse)
+    # planted mistake: the blocks come back in the wrong order
+    k3, v3 = cache.swap_in(kc, vc, kh, vh, new[::-1].copy())
+    w3 = W.Workload(**{**w.__dict__, "kv": W.PagedKV(k3, v3), "decode": d2})
+    bad, _ = oracle.decode(w3, requests=[0])
+    assert not np.allclose(bad[0], ref[0])
