@@ -87,6 +87,34 @@ def append_leg(torch, mp, W, np, dev, stream, flush, pk, rank, steps):
             "note": "bytes = new K and V rows read + pool rows written; pool and rows resident in HBM"}
 
 
+def offload_leg(torch, mp, np, dev, stream, flush, steps, n_blocks=1024):
+    """Time swapping n_blocks whole blocks (8 kv heads, d 128, bf16: 64 KiB of K
+    and V each) out to pinned host memory and back, beside one contiguous
+    device-to-host copy of the same bytes (the host link, for reference)."""
+    nblk = 4 * n_blocks
+    kp = torch.randn(nblk, 8, 16, 128, device=dev).to(torch.bfloat16)
+    vp = torch.randn_like(kp)
+    ids = torch.from_numpy(np.random.default_rng(0).choice(nblk, n_blocks, replace=False).astype(np.int32)).to(dev)
+    hk = torch.empty((n_blocks, 8, 16, 128), dtype=torch.bfloat16, pin_memory=True)
+    hv = torch.empty_like(hk, pin_memory=True)
+    out = lambda: mp.kv_swap_out(kp, vp, ids, hk, hv)
+    back = lambda: mp.kv_swap_in(hk, hv, ids, kp, vp)
+    src = torch.empty(2 * hk.numel(), dtype=torch.bfloat16, device=dev)
+    dst = torch.empty(2 * hk.numel(), dtype=torch.bfloat16, pin_memory=True)
+    link = lambda: dst.copy_(src, non_blocking=True)
+    res = {}
+    for name, fn in (("swap_out", out), ("swap_in", back), ("link_copy_d2h", link)):
+        for _ in range(3):
+            fn()
+        res[name] = statistics.median(timed(torch, stream, flush, fn, steps))
+    nbytes = 2 * hk.numel() * 2
+    return {"workload": f"{n_blocks} blocks of 8 kv heads x 16 x 128 bf16 (K and V), random ids",
+            "bytes": nbytes, **{k + "_ms": v for k, v in res.items()},
+            **{k + "_GB_s": nbytes / (v * 1e-3) / 1e9 for k, v in res.items()},
+            "note": "one gather/scatter kernel reaching pinned host memory directly; link_copy_d2h is one "
+                    "contiguous cudaMemcpyAsync of the same bytes"}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -495,6 +523,9 @@ def run_minipic(args):
         extras["kv_append"] = append_leg(torch, mp, W, np, dev, stream, flush, pk, rank, args.steps)
         if mp.device_error() != 0:
             raise RuntimeError("device error in kv_append")
+        extras["kv_offload"] = offload_leg(torch, mp, np, dev, stream, flush, args.steps)
+        if mp.device_error() != 0:
+            raise RuntimeError("device error in kv_offload")
 
         # mixed continuous batch: span prefills + decodes in ONE launch, against the parts run alone
         wm = W.mixed_batch(seed=rank)

@@ -284,6 +284,26 @@ typedef struct {
 minipic_status minipic_kv_append(minipic_dtype dtype, const minipic_kv_pool_mut* kv,
                                  const minipic_kv_append_batch* batch, minipic_stream_t stream);
 
+/* ------------------------------------------------------------------ host offload
+ * Moving whole blocks between the pools and host memory (MiniPIC summary,
+ * section 3, item 5: unrotated blocks move between GPU and host with no
+ * position to track or adjust).  A block's logical positions live in the
+ * requests' block_starts, so a block may come back to any free physical id:
+ * only the block tables change.
+ *
+ * host_k / host_v: page-locked host memory (cudaHostAlloc, cudaHostRegister or
+ * a pinned torch tensor) of n blocks, [n][num_kv_heads][block_size][head_dim]
+ * each, 16-byte aligned; the kernel reads or writes it directly over the
+ * host link.  block_ids: device int32 [n].  An id outside [0, num_blocks) sets
+ * MINIPIC_DEVERR_BLOCK_ID and that block is skipped.  Host memory that is not
+ * page-locked returns MINIPIC_ERR_INVALID.  Asynchronous on `stream`: the host
+ * buffer is complete (swap-out) or may be reused (swap-in) once the stream
+ * reaches this point.  Within a swap-in call the ids must be distinct. */
+minipic_status minipic_kv_swap_out(minipic_dtype dtype, const minipic_kv_pool* kv, const int32_t* block_ids,
+                                   int32_t n, void* host_k, void* host_v, minipic_stream_t stream);
+minipic_status minipic_kv_swap_in(minipic_dtype dtype, const minipic_kv_pool_mut* kv, const int32_t* block_ids,
+                                  int32_t n, const void* host_k, const void* host_v, minipic_stream_t stream);
+
 /* Read the device error word (MINIPIC_DEVERR_* bits, 0 if none) of the current
  * device after the work queued on `stream` has finished (this call
  * synchronizes the stream), and reset it to 0 when `clear` is nonzero.

@@ -129,6 +129,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                          ctypes.POINTER(_Prefill), ctypes.POINTER(_Decode), c_f, c_vp, c_sz, c_vp]
         L.minipic_kv_append.restype = ctypes.c_int
         L.minipic_kv_append.argtypes = [ctypes.c_int, ctypes.POINTER(_KV), ctypes.POINTER(_Append), c_vp]
+        for fn in (L.minipic_kv_swap_out, L.minipic_kv_swap_in):
+            fn.restype = ctypes.c_int
+            fn.argtypes = [ctypes.c_int, ctypes.POINTER(_KV), c_vp, c_i32, c_vp, c_vp, c_vp]
         L.minipic_device_error.restype = ctypes.c_int
         L.minipic_device_error.argtypes = [ctypes.POINTER(c_i32), c_i32, c_vp]
         _lib = L
@@ -402,3 +405,41 @@ def kv_append(k_new, v_new, cu_new_lens, kv_start, block_tables, k_pool, v_pool,
                  block_tables.data_ptr(), B, k_new.shape[0], int(max_new_len), block_tables.shape[1])
     _check(L.minipic_kv_append(_dtype_code(k_pool), ctypes.byref(kv), ctypes.byref(ab), _stream(stream)),
            "minipic_kv_append")
+
+
+def kv_swap_out(k_pool, v_pool, block_ids, host_k=None, host_v=None, stream=None):
+    """Copy whole blocks (K and V, every kv head) to page-locked host memory:
+    host[i] = pool[block_ids[i]].  Returns (host_k, host_v), allocated pinned
+    when not given; they are complete once the stream reaches this call."""
+    torch = _torch()
+    L = load()
+    kv = _kv(k_pool, v_pool)
+    _need(block_ids, "block_ids", dtype=torch.int32, ndim=1)
+    n = block_ids.shape[0]
+    shape = (n,) + tuple(k_pool.shape[1:])
+    if host_k is None:
+        host_k = torch.empty(shape, dtype=k_pool.dtype, pin_memory=True)
+    if host_v is None:
+        host_v = torch.empty(shape, dtype=k_pool.dtype, pin_memory=True)
+    for name, t in (("host_k", host_k), ("host_v", host_v)):
+        if tuple(t.shape) != shape or t.dtype != k_pool.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {tuple(shape)} tensor of the pool's dtype")
+    _check(L.minipic_kv_swap_out(_dtype_code(k_pool), ctypes.byref(kv), block_ids.data_ptr(), n,
+                                 host_k.data_ptr(), host_v.data_ptr(), _stream(stream)), "minipic_kv_swap_out")
+    return host_k, host_v
+
+
+def kv_swap_in(host_k, host_v, block_ids, k_pool, v_pool, stream=None):
+    """Copy host blocks back into the pools: pool[block_ids[i]] = host[i] (ids
+    need not be the ones the blocks left from; remap the block tables)."""
+    torch = _torch()
+    L = load()
+    kv = _kv(k_pool, v_pool)
+    _need(block_ids, "block_ids", dtype=torch.int32, ndim=1)
+    n = block_ids.shape[0]
+    shape = (n,) + tuple(k_pool.shape[1:])
+    for name, t in (("host_k", host_k), ("host_v", host_v)):
+        if tuple(t.shape) != shape or t.dtype != k_pool.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {tuple(shape)} tensor of the pool's dtype")
+    _check(L.minipic_kv_swap_in(_dtype_code(k_pool), ctypes.byref(kv), block_ids.data_ptr(), n,
+                                host_k.data_ptr(), host_v.data_ptr(), _stream(stream)), "minipic_kv_swap_in")

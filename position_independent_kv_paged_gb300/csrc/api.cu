@@ -422,6 +422,66 @@ minipic_status minipic_kv_append(minipic_dtype dtype, const minipic_kv_pool_mut*
   return launch_kv_append(a, (cudaStream_t)stream) == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 
+namespace {
+
+// Device-side address of page-locked host memory (nullptr if it is not).
+void* host_device_ptr(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky error of a failed query
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  return at.devicePointer;
+}
+
+minipic_status offload(minipic_dtype dtype, void* k_pool, void* v_pool, int32_t num_blocks, int32_t Hkv,
+                       int32_t bs, int32_t D, const int32_t* ids, int32_t n, const void* host_k,
+                       const void* host_v, bool to_host, cudaStream_t stream) {
+  if (dtype != MINIPIC_F32 && dtype != MINIPIC_BF16) return MINIPIC_ERR_INVALID;
+  if (num_blocks < 0 || Hkv <= 0 || bs <= 0 || D <= 0 || n < 0) return MINIPIC_ERR_INVALID;
+  if (D != 64 && D != 128) return MINIPIC_ERR_UNSUPPORTED;
+  if (bs != 16) return MINIPIC_ERR_UNSUPPORTED;
+  if (n == 0) return MINIPIC_OK;
+  if (num_blocks == 0 || !k_pool || !v_pool || !ids || !host_k || !host_v) return MINIPIC_ERR_INVALID;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(host_k) || !aligned16(host_v))
+    return MINIPIC_ERR_INVALID;
+  void* dk = host_device_ptr(host_k);
+  void* dv = host_device_ptr(host_v);
+  if (!dk || !dv || !aligned16(dk) || !aligned16(dv)) return MINIPIC_ERR_INVALID;
+  int* err = nullptr;
+  int sms = 0;
+  if (device_info(&err, &sms) != cudaSuccess) return MINIPIC_ERR_CUDA;
+  OffloadArgs a{};
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.host_k = dk;
+  a.host_v = dv;
+  a.block_ids = ids;
+  a.n = n;
+  a.num_blocks = num_blocks;
+  a.block_chunks = (long long)Hkv * bs * D * (dtype == MINIPIC_BF16 ? 2 : 4) / 16;
+  a.err = err;
+  return launch_kv_offload(a, to_host, sms, stream) == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
+}  // namespace
+
+minipic_status minipic_kv_swap_out(minipic_dtype dtype, const minipic_kv_pool* kv, const int32_t* block_ids,
+                                   int32_t n, void* host_k, void* host_v, minipic_stream_t stream) {
+  if (!kv) return MINIPIC_ERR_INVALID;
+  return offload(dtype, const_cast<void*>(kv->k_pool), const_cast<void*>(kv->v_pool), kv->num_blocks,
+                 kv->num_kv_heads, kv->block_size, kv->head_dim, block_ids, n, host_k, host_v, true,
+                 (cudaStream_t)stream);
+}
+
+minipic_status minipic_kv_swap_in(minipic_dtype dtype, const minipic_kv_pool_mut* kv, const int32_t* block_ids,
+                                  int32_t n, const void* host_k, const void* host_v, minipic_stream_t stream) {
+  if (!kv) return MINIPIC_ERR_INVALID;
+  return offload(dtype, kv->k_pool, kv->v_pool, kv->num_blocks, kv->num_kv_heads, kv->block_size, kv->head_dim,
+                 block_ids, n, host_k, host_v, false, (cudaStream_t)stream);
+}
+
 minipic_status minipic_device_error(int32_t* flags_out, int32_t clear, minipic_stream_t stream) {
   int* err = nullptr;
   if (device_info(&err, nullptr) != cudaSuccess) return MINIPIC_ERR_CUDA;

@@ -84,6 +84,19 @@ struct AppendArgs {
 };
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t s);
 
+// Whole-block copies between the pools and page-locked host memory.
+struct OffloadArgs {
+  void* k_pool;  // [num_blocks][Hkv][16][D]
+  void* v_pool;
+  void* host_k;  // device-side address of the host buffer, [n][Hkv][16][D]
+  void* host_v;
+  const int32_t* block_ids;  // [n]
+  int n, num_blocks;
+  long long block_chunks;  // 16-byte chunks of one block (all kv heads)
+  int* err;
+};
+cudaError_t launch_kv_offload(const OffloadArgs& a, bool to_host, int num_sms, cudaStream_t s);
+
 // Byte layout of the decode workspace: one completion counter per (request,
 // kv head) first, then partial outputs and partial (max, sum) pairs.
 struct DecodeWs {

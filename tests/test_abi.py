@@ -116,3 +116,15 @@ def test_kv_append_validation(lib):
     assert f(1, ctypes.byref(kv), ctypes.byref(bad), None) == 1              # negative batch
     nulls = App(None, None, None, None, None, 2, 5, 3, 1)
     assert f(1, ctypes.byref(kv), ctypes.byref(nulls), None) == 1            # missing pointers
+
+
+def test_kv_swap_validation(lib):
+    KV = mp._KV
+    for f in (lib.minipic_kv_swap_out, lib.minipic_kv_swap_in):
+        kv = KV(None, None, 4, 2, 16, 128)
+        assert f(1, ctypes.byref(kv), None, 0, None, None, None) == 0      # nothing to move
+        assert f(9, ctypes.byref(kv), None, 0, None, None, None) == 1      # bad dtype
+        assert f(1, None, None, 1, None, None, None) == 1                  # no pool
+        assert f(1, ctypes.byref(KV(None, None, 4, 2, 16, 80)), None, 1, None, None, None) == 2
+        assert f(1, ctypes.byref(kv), None, -1, None, None, None) == 1     # negative count
+        assert f(1, ctypes.byref(kv), None, 3, None, None, None) == 1      # missing pointers
