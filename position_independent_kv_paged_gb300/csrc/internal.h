@@ -67,6 +67,8 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, bool bf16, bool rotate, cuda
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool rotate, cudaStream_t s);
 cudaError_t launch_decode_merge(const DecodeArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, bool rotate, cudaStream_t s);
+// Head dim 128: CTA-pair (cta_group::2) form, called by launch_prefill_tc.
+cudaError_t launch_prefill_pair(const PrefillArgs& a, bool rotate, cudaStream_t s);
 // One grid of prefill tiles followed by decode splits (both with rotation).
 cudaError_t launch_mixed(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s);
 

@@ -50,6 +50,7 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, bool rotate, cudaStream_t s) {
+  if (a.D == 128) return launch_prefill_pair(a, rotate, s);
   if (rotate) return a.D == 128 ? launch_t<128, true>(a, s) : launch_t<64, true>(a, s);
   return a.D == 128 ? launch_t<128, false>(a, s) : launch_t<64, false>(a, s);
 }
