@@ -32,8 +32,10 @@
 //   warp 12     K~ producer: this CTA's K~ blocks and block-start cos/sin
 //               rows by TMA, and the tile's key masks and V block ids
 //   warp 13     TMEM allocation; in CTA 0 the MMA issue, in CTA 1 a relay
-//               that tells CTA 0 when its V stage has landed
-//   warp 14     V producer: this CTA's 64 head dims of every V block by TMA
+//               that tells CTA 0 when its rotated keys are ready (one
+//               cluster-scope release per tile, covering what it observed)
+//   warp 14     V producer: this CTA's 64 head dims of every V block by TMA;
+//               both CTAs' copies complete on CTA 0's V barrier
 // (K~ and V have producers of their own, so that K~ tiles run NSK tiles ahead
 // of the products whatever the V stages wait for.)
 // S is double-buffered in TMEM, so QK^T of tile t+1 runs while the softmax
@@ -88,9 +90,10 @@ struct PP {
   static constexpr int OFF_FLAG = OFF_RED + 2 * 2 * 128 * 4;      // [2][2][4] int
   static constexpr int B_KFULL = 0, B_VFULL = B_KFULL + NSK, B_KFREE = B_VFULL + NSV, B_VFREE = B_KFREE + NSK;
   static constexpr int B_S = B_VFREE + NSV, B_PV = B_S + 2, B_MASK = B_PV + 1;
-  // arrived on in CTA 0 only (by both CTAs)
-  static constexpr int B_QRDY = B_MASK + kMaskRing, B_KROT = B_QRDY + 1, B_VPEER = B_KROT + NSK;
-  static constexpr int B_P = B_VPEER + NSV, NBARS = B_P + 2;
+  // B_KROTL: this CTA's rotation warps; B_KROT: CTA 1's relay (in CTA 0);
+  // B_QRDY, B_P: both CTAs' warps; B_VFULL: both CTAs' V copies (used in CTA 0)
+  static constexpr int B_QRDY = B_MASK + kMaskRing, B_KROT = B_QRDY + 1;
+  static constexpr int B_P = B_KROT + NSK, B_KROTL = B_P + 2, NBARS = B_KROTL + NSK;
   static constexpr int OFF_BAR = (OFF_FLAG + 2 * 2 * 4 * 4 + 15) / 16 * 16;
   static constexpr int OFF_TSLOT = OFF_BAR + NBARS * 8;
   static constexpr int TOTAL = OFF_TSLOT + 16;
@@ -130,10 +133,9 @@ __device__ __forceinline__ void rot_pack(U4& x, U4& y, const uint64_t (&c2)[4], 
   y = U4{yw[0], yw[1], yw[2], yw[3]};
 }
 
-// Arrive on barrier `bar` of CTA 0 of the pair (locally in CTA 0).  No
-// cluster-scope fence: the arrivals stand for TMEM stores already waited on or
-// shared-memory writes already published to the async proxy, which CTA 0's
-// tensor-core operations read.
+// Arrive on barrier `bar` of CTA 0 of the pair (locally in CTA 0) for TMEM
+// stores already waited on (tcgen05.wait::st and tcgen05.fence before the
+// arrival), which CTA 0's tensor-core operations read.
 __device__ __forceinline__ void arrive_leader(uint32_t bar, uint32_t crank) {
   if (crank == 0) ptx::mbar_arrive(bar);
   else ptx::mbar_arrive_peer(bar, 0);
@@ -183,12 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NSK; ++s) {
       ptx::mbar_init(bar(P_::B_KFULL + s), 1);
       ptx::mbar_init(bar(P_::B_KFREE + s), 1);
-      ptx::mbar_init(bar(P_::B_KROT + s), 8);  // four rotation warps in each CTA
+      ptx::mbar_init(bar(P_::B_KROT + s), 1);   // CTA 1's relay
+      ptx::mbar_init(bar(P_::B_KROTL + s), 4);  // this CTA's four rotation warps
     }
     for (int s = 0; s < NSV; ++s) {
-      ptx::mbar_init(bar(P_::B_VFULL + s), 1);
+      ptx::mbar_init(bar(P_::B_VFULL + s), 2);  // one producer arrival from each CTA
       ptx::mbar_init(bar(P_::B_VFREE + s), 1);
-      ptx::mbar_init(bar(P_::B_VPEER + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(P_::B_S + i), 1);
@@ -296,7 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kVWarp) {
     // ======================================================== V producer
     // V tile t (this CTA's 64 head dims of all ten blocks) once PV(t - NSV)
-    // freed the stage and the K~ producer published the tile's block ids.
+    // freed the stage and the K~ producer published the tile's block ids.  The
+    // copies complete on CTA 0's barrier (CTA 1's through the cta_group::2 form),
+    // so the tensor core that reads both halves waits on one barrier.
+    const uint32_t vfull0 = ptx::mapa(bar(P_::B_VFULL), 0);  // CTA 0's barrier, cluster address
     bool ok = true;
     for (int t = 0; t < n_kt; ++t) {
       const int sv = t % NSV;
@@ -308,24 +313,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
       const int ph = lane < kTileBlocks ? vblk[(t % kMaskRing) * kTileBlocks + lane] : -1;
       const unsigned vv = __ballot_sync(FULL, ph >= 0);
-      if (lane == 0) ptx::mbar_arrive_expect_tx(bar(P_::B_VFULL + sv), __popc(vv) * 2048);
+      const uint32_t vbar = vfull0 + 8u * (uint32_t)sv;
+      if (lane == 0) ptx::mbar_arrive_expect_tx_cl(vbar, __popc(vv) * 2048);
       __syncwarp();
       if (ph >= 0)
-        ptx::tma_load_2d(sbase + P_::OFF_V + sv * P_::VTILE + lane * 2048, &vmap, 64 * (int)crank,
-                         (ph * a.Hkv + hk) * 16, bar(P_::B_VFULL + sv));
+        ptx::tma_load_2d_pair(sbase + P_::OFF_V + sv * P_::VTILE + lane * 2048, &vmap, 64 * (int)crank,
+                              (ph * a.Hkv + hk) * 16, vbar);
     }
     if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
     __syncwarp();
   } else if (warp == kMmaWarp && crank != 0) {
-    // ======================================================== V relay (CTA 1)
-    // CTA 0 issues the products, so it must know when this CTA's V stage landed.
+    // ======================================================== relay (CTA 1)
+    // CTA 0 issues the products, which read the keys this CTA's threads rotated
+    // in place.  The relay observes each tile's rotation with an acquire and
+    // forwards it with a release at cluster scope.
     if (lane == 0) {
-      for (int t = 0; t < n_kt; ++t) {
-        if (!ptx::mbar_wait(bar(P_::B_VFULL + t % NSV), (t / NSV) & 1)) {
+      for (int u = 0; u < n_kt; ++u) {
+        if (!ptx::mbar_wait(bar(P_::B_KROTL + u % NSK), (u / NSK) & 1)) {
           atomicOr(a.err, kErrTimeout);
           break;
         }
-        ptx::mbar_arrive_peer(bar(P_::B_VPEER + t % NSV), 0);
+        ptx::mbar_arrive_remote(bar(P_::B_KROT + u % NSK), 0);
       }
     }
     __syncwarp();
@@ -339,7 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // stage is released to both producers while a later tile refills it
       auto qk = [&](int t) -> bool {
         const int s = t % NSK;
-        if (!ptx::mbar_wait(bar(P_::B_KROT + s), (t / NSK) & 1)) return false;
+        if (!ptx::mbar_wait(bar(P_::B_KROTL + s), (t / NSK) & 1) ||
+            !ptx::mbar_wait_cl(bar(P_::B_KROT + s), (t / NSK) & 1))
+          return false;
         umma::fence_after_sync();
         const uint32_t kb = sbase + P_::OFF_K + s * P_::KTILE;
 #pragma unroll
@@ -357,8 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < n_kt && ok; ++t) {
         const int sv = t % NSV;
         if (!ptx::mbar_wait(bar(P_::B_P + (t & 1)), (t >> 1) & 1) ||
-            !ptx::mbar_wait(bar(P_::B_VFULL + sv), (t / NSV) & 1) ||
-            !ptx::mbar_wait(bar(P_::B_VPEER + sv), (t / NSV) & 1)) {
+            !ptx::mbar_wait(bar(P_::B_VFULL + sv), (t / NSV) & 1)) {
           ok = false;
           break;
         }
@@ -513,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) arrive_leader(bar(P_::B_KROT + s), crank);
+      if (lane == 0) ptx::mbar_arrive(bar(P_::B_KROTL + s));
     }
   } else if (warp < kSoftWarps) {
     // ======================================================== softmax

@@ -176,6 +176,31 @@ __device__ __forceinline__ void mbar_arrive_peer(uint32_t bar, uint32_t rank) {
       : "memory");
 }
 
+// 2-D tiled TMA load into this CTA's shared memory whose completion (bytes) is
+// signalled on an mbarrier of the CTA pair's even CTA (cta_group::2 form):
+// `bar_cl` is that barrier's shared::cluster address (mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cl) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cl)
+      : "memory");
+}
+// shared::cluster address of local shared offset `addr` in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive (relaxed) on a barrier given by its shared::cluster address and add
+// `bytes` to the transaction count its phase expects.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cl(uint32_t bar_cl, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cl),
+               "r"(bytes)
+               : "memory");
+}
+
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
