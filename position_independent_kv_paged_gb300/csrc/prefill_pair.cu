@@ -27,8 +27,8 @@
 //   warps 0-7   softmax: warp w covers TMEM lanes 32 (w % 4).. (query rows)
 //               and keys 80 (w / 4) .. +79 of the tile; the two warps of a
 //               lane quarter combine their row maxima through shared memory
-//   warps 8-11  query preparation (rotated, scaled query into TMEM), then
-//               rotation of this CTA's 80 keys of every staged tile
+//   warps 8-11  rotation of this CTA's 80 keys of every staged tile
+// (warps 0-3 first prepare the rotated, scaled query tile in TMEM)
 //   warp 12     K~ producer: this CTA's K~ blocks and block-start cos/sin
 //               rows by TMA, and the tile's key masks and V block ids
 //   warp 13     TMEM allocation; in CTA 0 the MMA issue, in CTA 1 a relay
@@ -169,6 +169,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ql = a.cu_q_lens[r + 1] - q0;
   const int tok0 = (2 * pair + (int)crank) * TQ;  // first token of this CTA's query tile
   if (tid == 0 && crank == 0 && pair == L.n_pairs - 1 && ql > L.n_pairs * 2 * TQ) atomicOr(a.err, kErrSeqLen);
+
+  // Loads whose latency the setup below hides: the rotation warps' cos/sin of
+  // the slot angles, warps 0-3's query row and its position, and the K~
+  // producer's table entries of the first tile.
+  uint64_t rsc[4], rss[4];
+  if (ROPE && tid >= kRotBase && tid < kRotBase + kRotThreads) {
+    const int fg = (tid - kRotBase) & 7, sl = (tid - kRotBase) >> 3;
+    const float* tr = a.cos_sin + (size_t)min(sl, a.max_pos - 1) * D;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 c = __ldg(reinterpret_cast<const float2*>(tr + 8 * fg + 2 * e));
+      const float2 sn = __ldg(reinterpret_cast<const float2*>(tr + D / 2 + 8 * fg + 2 * e));
+      rsc[e] = ptx::f2(c.x, c.y);
+      rss[e] = ptx::f2(sn.x, sn.y);
+    }
+  }
+  U4 qc[D / 8];
+  int qpos = 0;
+  if (tid < 128) {  // query row tid of this CTA's tile
+    const int rtok = tid / G, rh = tid - rtok * G;
+    const int tq = tok0 + rtok;
+    if (rtok < TQ && tq < ql) {
+      const __nv_bfloat16* qp =
+          static_cast<const __nv_bfloat16*>(a.q) + ((size_t)(q0 + tq) * a.Hq + (size_t)hk * G + rh) * D;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qp) + c);
+        qc[c] = U4{v.x, v.y, v.z, v.w};
+      }
+      if (ROPE) qpos = a.q_pos[q0 + tq];
+    } else {
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) qc[c] = U4{0u, 0u, 0u, 0u};
+    }
+  }
+  int pre_ph = -1, pre_st = 0;
+  if (warp == kTmaWarp && lane < kTileBlocks && lane < mb) {
+    pre_ph = __ldg(a.block_tables + (size_t)r * mb + lane);
+    pre_st = __ldg(a.block_starts + (size_t)r * mb + lane);
+  }
   if (ql <= 0 || 2 * pair * TQ >= ql) return;  // decided alike in both CTAs of the pair
   int kvl = a.kv_lens[r];
   if (kvl < ql || kvl > mb * 16) {
@@ -205,9 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma2::tmem_alloc(ptx::smem_addr(tslot), kTCols);
     umma2::tmem_relinquish();
   }
-  // zero the K and V stages once so that never-loaded blocks hold finite values
-  for (int i = tid; i < (NSK * P_::KTILE + NSV * P_::VTILE) / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sg + P_::OFF_K)[i] = make_uint4(0u, 0u, 0u, 0u);
+  // zero the V stages once so that never-loaded blocks hold finite values (a
+  // masked key's P is 0, which must not meet an Inf or NaN in V; masked scores
+  // are replaced, so K~ stages need no clearing)
+  for (int i = tid; i < NSV * P_::VTILE / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sg + P_::OFF_V)[i] = make_uint4(0u, 0u, 0u, 0u);
   ptx::fence_proxy_async_smem();
   umma::fence_before_sync();
   __syncthreads();
@@ -237,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         my_st = in ? __ldg(bs + b) : 0;
       };
       bool ok = true;
-      fetch(0);
+      my_ph = lane < kTileBlocks && lane < nblk ? pre_ph : -1;  // tile 0, loaded before the setup
+      my_st = lane < kTileBlocks && lane < nblk ? pre_st : 0;
       for (int u = 0; u < n_kt; ++u) {
         {
           const int s = u % NSK;
@@ -386,97 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (tid >= kRotBase) {
-    // ======================================================== query preparation + key rotation
-    const int rt = tid - kRotBase;  // 0..127 = TMEM lane (warp 8 + i covers lanes 32 i ..)
-    const float qs = a.scale * kLog2e;
-    {
-      // ---- query row rt: rotated at its position, scaled by scale * log2(e),
-      // packed (f16 with rotation, bf16 without) into TMEM columns as the A operand
-      const int rtok = rt / G, rh = rt - rtok * G;
-      const int tq = tok0 + rtok;
-      const bool row_ok = rtok < TQ && tq < ql;
-      U4 qc[D / 8];
-      int pos = 0;
-      if (row_ok) {
-        const __nv_bfloat16* qp =
-            static_cast<const __nv_bfloat16*>(a.q) + ((size_t)(q0 + tq) * a.Hq + (size_t)hk * G + rh) * D;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qp) + c);
-          qc[c] = U4{v.x, v.y, v.z, v.w};
-        }
-        if (ROPE) {
-          pos = a.q_pos[q0 + tq];
-          if (pos < 0 || pos >= a.max_pos) {
-            atomicOr(a.err, kErrPosition);
-            pos = 0;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) qc[c] = U4{0u, 0u, 0u, 0u};
-      }
-      if constexpr (ROPE) {
-        const float* trow = a.cos_sin + (size_t)pos * D;
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) {  // chunk c pairs with chunk c + D/16
-          uint64_t c2[4], s2[4];
-          const float4 ca = __ldg(reinterpret_cast<const float4*>(trow + 8 * c));
-          const float4 cb = __ldg(reinterpret_cast<const float4*>(trow + 8 * c + 4));
-          const float4 sa = __ldg(reinterpret_cast<const float4*>(trow + D / 2 + 8 * c));
-          const float4 sb = __ldg(reinterpret_cast<const float4*>(trow + D / 2 + 8 * c + 4));
-          c2[0] = ptx::f2(ca.x * qs, ca.y * qs); c2[1] = ptx::f2(ca.z * qs, ca.w * qs);
-          c2[2] = ptx::f2(cb.x * qs, cb.y * qs); c2[3] = ptx::f2(cb.z * qs, cb.w * qs);
-          s2[0] = ptx::f2(sa.x * qs, sa.y * qs); s2[1] = ptx::f2(sa.z * qs, sa.w * qs);
-          s2[2] = ptx::f2(sb.x * qs, sb.y * qs); s2[3] = ptx::f2(sb.z * qs, sb.w * qs);
-          rot_pack(qc[c], qc[c + D / 16], c2, s2);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          U4& x = qc[c];
-          x = U4{ptx::pack_bf16(ptx::bf_lo(x.x) * qs, ptx::bf_hi(x.x) * qs),
-                 ptx::pack_bf16(ptx::bf_lo(x.y) * qs, ptx::bf_hi(x.y) * qs),
-                 ptx::pack_bf16(ptx::bf_lo(x.z) * qs, ptx::bf_hi(x.z) * qs),
-                 ptx::pack_bf16(ptx::bf_lo(x.w) * qs, ptx::bf_hi(x.w) * qs)};
-        }
-      }
-      // column j holds head dims 2 j, 2 j + 1
-      const uint32_t tq_addr = tmem + kColQ + ((uint32_t)(32 * (warp - 8)) << 16);
-#pragma unroll
-      for (int part = 0; part < D / 32; ++part) {
-        uint32_t w[16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const U4& x = qc[4 * part + c];
-          w[4 * c] = x.x;
-          w[4 * c + 1] = x.y;
-          w[4 * c + 2] = x.z;
-          w[4 * c + 3] = x.w;
-        }
-        umma::tmem_st16(tq_addr + 16 * part, w);
-      }
-      umma::tmem_wait_st();
-      umma::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) arrive_leader(bar(P_::B_QRDY), crank);
-    }
-
+    // ======================================================== key rotation
+    const int rt = tid - kRotBase;  // 0..127
     // ---- key rotation: thread -> (frequency group fg of 8, slot sl): slot sl
     // of this CTA's five blocks; cos/sin(sl theta_f), f = 8 fg .. 8 fg + 7, stay
     // in registers and the block start's come from the staged table rows
-    const int fg = rt & 7, sl = rt >> 3;
-    uint64_t rsc[4], rss[4];
-    if constexpr (ROPE) {
-      const float* tr = a.cos_sin + (size_t)min(sl, a.max_pos - 1) * D;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 c = __ldg(reinterpret_cast<const float2*>(tr + 8 * fg + 2 * e));
-        const float2 sn = __ldg(reinterpret_cast<const float2*>(tr + D / 2 + 8 * fg + 2 * e));
-        rsc[e] = ptx::f2(c.x, c.y);
-        rss[e] = ptx::f2(sn.x, sn.y);
-      }
-    }
+    const int fg = rt & 7, sl = rt >> 3;  // rsc / rss: loaded before the setup
     const int key0 = (int)crank * BH;  // this CTA's first key of a tile
     for (int t = 0; t < n_kt; ++t) {
       const int s = t % NSK;
@@ -543,6 +501,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t nb_id = 1 + qd;  // named barrier of warps qd, qd + 4
     float m_run = -CUDART_INF_F, m_use = -CUDART_INF_F, l_run = 0.f;
     bool failed = false, pv_late = false;
+    if (h == 0) {
+      const float qs = a.scale * kLog2e;
+      // ---- query row `row` (warps 0-3, while the rotation warps start on the
+      // first key tile): rotated at its position, scaled by scale * log2(e),
+      // packed (f16 with rotation, bf16 without) into TMEM columns as the A operand
+      
+      // qc and qpos (row tid = row) were loaded before the setup
+      int pos = qpos;
+      if (ROPE && row_ok && (pos < 0 || pos >= a.max_pos)) {
+        atomicOr(a.err, kErrPosition);
+        pos = 0;
+      }
+      if constexpr (ROPE) {
+        const float* trow = a.cos_sin + (size_t)pos * D;
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {  // chunk c pairs with chunk c + D/16
+          uint64_t c2[4], s2[4];
+          const float4 ca = __ldg(reinterpret_cast<const float4*>(trow + 8 * c));
+          const float4 cb = __ldg(reinterpret_cast<const float4*>(trow + 8 * c + 4));
+          const float4 sa = __ldg(reinterpret_cast<const float4*>(trow + D / 2 + 8 * c));
+          const float4 sb = __ldg(reinterpret_cast<const float4*>(trow + D / 2 + 8 * c + 4));
+          c2[0] = ptx::f2(ca.x * qs, ca.y * qs); c2[1] = ptx::f2(ca.z * qs, ca.w * qs);
+          c2[2] = ptx::f2(cb.x * qs, cb.y * qs); c2[3] = ptx::f2(cb.z * qs, cb.w * qs);
+          s2[0] = ptx::f2(sa.x * qs, sa.y * qs); s2[1] = ptx::f2(sa.z * qs, sa.w * qs);
+          s2[2] = ptx::f2(sb.x * qs, sb.y * qs); s2[3] = ptx::f2(sb.z * qs, sb.w * qs);
+          rot_pack(qc[c], qc[c + D / 16], c2, s2);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          U4& x = qc[c];
+          x = U4{ptx::pack_bf16(ptx::bf_lo(x.x) * qs, ptx::bf_hi(x.x) * qs),
+                 ptx::pack_bf16(ptx::bf_lo(x.y) * qs, ptx::bf_hi(x.y) * qs),
+                 ptx::pack_bf16(ptx::bf_lo(x.z) * qs, ptx::bf_hi(x.z) * qs),
+                 ptx::pack_bf16(ptx::bf_lo(x.w) * qs, ptx::bf_hi(x.w) * qs)};
+        }
+      }
+      // column j holds head dims 2 j, 2 j + 1
+      const uint32_t tq_addr = tmem + kColQ + lane_base;
+#pragma unroll
+      for (int part = 0; part < D / 32; ++part) {
+        uint32_t w[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const U4& x = qc[4 * part + c];
+          w[4 * c] = x.x;
+          w[4 * c + 1] = x.y;
+          w[4 * c + 2] = x.z;
+          w[4 * c + 3] = x.w;
+        }
+        umma::tmem_st16(tq_addr + 16 * part, w);
+      }
+      umma::tmem_wait_st();
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) arrive_leader(bar(P_::B_QRDY), crank);
+    }
+
     int rounds = 0;
     auto exchange = [&](float mine, bool ok, float& other, bool& other_ok) {
       const int p = rounds & 1;
@@ -700,12 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       a.lse[(size_t)(q0 + tq) * a.Hq + hq] = l_tot > 0.f ? (m_use + log2f(l_tot)) * kLn2 : -CUDART_INF_F;
   }
 
+  // teardown: execution barriers only (nothing left to publish)
   umma::fence_before_sync();
   __syncthreads();
-  ptx::cluster_sync();  // every product of the pair has completed and been read
+  ptx::cluster_sync_relaxed();  // every product of the pair has completed and been read
   umma::fence_after_sync();
   if (warp == kMmaWarp) umma2::tmem_dealloc(tmem, kTCols);
-  ptx::cluster_sync();  // neither CTA leaves while the pair's TMEM is being released
+  ptx::cluster_sync_relaxed();  // neither CTA leaves while the pair's TMEM is being released
 }
 
 template <bool ROPE>
