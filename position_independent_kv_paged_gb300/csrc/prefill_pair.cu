@@ -21,14 +21,15 @@
 // the size a single CTA would hold.  With A in TMEM an MMA costs about
 // max(93, 9.5 + N / 2) SM cycles (measured), so a 160-wide QK^T product runs
 // near the tensor core's peak, where the shared-memory form at 96 keys ran at
-// two thirds of it.
+// two thirds of it.  Every stage and barrier lives in both CTAs at the same
+// offsets; CTA 0's barriers gather what its tensor core waits for.
 //
-// Roles in each CTA (14 warps):
+// Roles in each CTA (15 warps):
 //   warps 0-7   softmax: warp w covers TMEM lanes 32 (w % 4).. (query rows)
 //               and keys 80 (w / 4) .. +79 of the tile; the two warps of a
-//               lane quarter combine their row maxima through shared memory
+//               lane quarter combine their row maxima through shared memory;
+//               warps 0-3 first write the rotated, scaled query tile to TMEM
 //   warps 8-11  rotation of this CTA's 80 keys of every staged tile
-// (warps 0-3 first prepare the rotated, scaled query tile in TMEM)
 //   warp 12     K~ producer: this CTA's K~ blocks and block-start cos/sin
 //               rows by TMA, and the tile's key masks and V block ids
 //   warp 13     TMEM allocation; in CTA 0 the MMA issue, in CTA 1 a relay

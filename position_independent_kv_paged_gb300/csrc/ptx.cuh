@@ -85,10 +85,6 @@ __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, uint
   }
   return true;
 }
-// Arrive (release, cluster scope) on the mbarrier at local offset bar of this CTA.
-__device__ __forceinline__ void mbar_arrive_cl(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

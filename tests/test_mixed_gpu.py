@@ -63,8 +63,11 @@ def test_mixed_equals_separate_calls(env):
     sd, _ = mp.attn_decode(dec["q"], kpool, vpool, dec["block_tables"], dec["block_starts"], dec["seq_lens"],
                            dec["q_pos"], rope)
     torch.cuda.synchronize()
-    # the prefill tiles run the same CTA body as the standalone kernel: identical bits
-    assert np.array_equal(so.float().cpu().numpy(), po)
+    # for head dim 128 the standalone prefill is the CTA-pair kernel (160-key tiles)
+    # and the mixed grid runs the single-CTA body (96-key tiles): the same sums in
+    # another order, so equal up to rounding (a bf16 ulp is 2^-7 relative)
+    pdiff = np.abs(so.float().cpu().numpy() - po)
+    assert pdiff.max() <= 2e-2 and pdiff.mean() <= 5e-4, (pdiff.max(), pdiff.mean())
     # decode CTAs in the mixed grid spread a split over 12 warps instead of 4, which
     # groups the per-warp partial sums differently: equal up to rounding
     diff = np.abs(sd.float().cpu().numpy() - do)
