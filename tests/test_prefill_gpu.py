@@ -121,3 +121,32 @@ def test_prerotated_prefill_equals_oracle_on_private_copies(env):
                                         t["block_tables"], t["block_starts"], t["kv_lens"], max_q_len=200)
     torch.cuda.synchronize()
     compare(out.float().cpu().numpy(), ref, "bf16", "prerotated prefill")
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (12, 4, 64)])
+def test_prefill_with_empty_chunks(env, Hq, Hkv, d):
+    """Requests without query tokens sit between others: their query-tile pairs
+    do nothing and the other requests' rows are unaffected."""
+    w = W.irregular_prefill(40 + d, "bf16", kv_lens=[16, 40, 700, 5, 64, 9], q_lens=[0, 1, 333, 0, 64, 9], Hq=Hq,
+                            Hkv=Hkv, d=d, max_pos=30000)
+    out, lse = run_prefill(env, w)
+    ref, rl = oracle.prefill(w)
+    compare(out, ref, "bf16", f"prefill with empty chunks {Hq}/{Hkv}/{d}")
+    compare_lse(lse, rl, "bf16", "prefill with empty chunks")
+    assert env[1].device_error() == 0
+
+
+@pytest.mark.parametrize("case", ["rag", "short_items"])
+def test_prefill_repeats_bit_for_bit(env, case):
+    """Every launch computes the same sums in the same order, so repeated calls
+    agree bit for bit; a race between the two CTAs of a pair (an operand read
+    before its writer finished) shows up here as a difference between calls."""
+    if case == "rag":
+        w = W.rag_prefill(3, B=4, n_spans=3, span_tokens=512, pool_spans=8, q_len=300)
+    else:  # many query-tile pairs with one or two key tiles each
+        w = W.mixed_batch(7, n_prefill=6, chunk=300, n_decode=0, Hq=28, Hkv=4)
+    first, first_lse = run_prefill(env, w)
+    for _ in range(4):
+        out, lse = run_prefill(env, w)
+        assert np.array_equal(out, first) and np.array_equal(lse, first_lse, equal_nan=True)
+    assert env[1].device_error() == 0
