@@ -512,6 +512,8 @@ def run_minipic(args):
         tf = cp.flops / (mp_ * 1e-3) / 1e12
         extras["prefill"] = {"workload": f"{wp.name}: {wp.notes}", "ms_per_step": mp_, "TFLOP_s": tf,
                              "frac_of_bf16_peak": tf / pk["bf16"], "peak_TFLOP_s": pk["bf16"],
+                             "frac_of_bf16_sustained": tf / pk["bf16_sus"],
+                             "sustained_peak_TFLOP_s": pk["bf16_sus"],
                              "algorithmic_flops": cp.flops, "rope_off_ms": mpn, "rope_overhead": mp_ / mpn - 1.0}
         if mp.device_error() != 0:
             raise RuntimeError("device error in prefill")
