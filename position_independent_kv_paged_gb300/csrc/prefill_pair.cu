@@ -603,6 +603,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < BH; j += 2)
           pm[(j >> 1) & 3] = ptx::fmax3(pm[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
         mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+      } else if (ok && mall == 0xffffu) {
+        // every block usable: the valid keys are the causal prefix j < nv
+        const int nv = row_ok ? lim - kb0 + 1 : 0;
+#pragma unroll
+        for (int j = 0; j < BH; ++j) {
+          v[j] = j < nv ? v[j] : __float_as_uint(-CUDART_INF_F);
+          mx = fmaxf(mx, __uint_as_float(v[j]));
+        }
       } else if (ok) {
         // invalid keys become -inf in place, so that both passes treat them alike
 #pragma unroll
