@@ -578,6 +578,15 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
         for (int j = 0; j < BN; j += 2)
           pm[(j >> 1) & 3] = ptx::fmax3(pm[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
         mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+      } else if (mall == 0xffffffffu) {
+        // every block usable: the valid keys are the causal prefix j < nv
+        const int nv = row_ok ? lim - kb0 + 1 : 0;
+        mx = -CUDART_INF_F;
+#pragma unroll
+        for (int j = 0; j < BN; ++j) {
+          v[j] = j < nv ? v[j] : __float_as_uint(-CUDART_INF_F);
+          mx = fmaxf(mx, __uint_as_float(v[j]));
+        }
       } else {
         // invalid keys become -inf in place, so that both passes treat them alike
         mx = -CUDART_INF_F;
