@@ -117,6 +117,25 @@ __device__ __forceinline__ void rotate_pair(U4& x, U4& y, const uint64_t (&c2)[4
   y = U4{yw[0], yw[1], yw[2], yw[3]};
 }
 
+// The same rotation for key rows by the slot angle, in packed bf16 arithmetic:
+//   x' = bf16(y (-s) + bf16(x c)),  y' = bf16(x s + bf16(y c))
+// (c, s, -s as bf16 pairs).  The keys feed a bf16 product, so they are rounded
+// to bf16 anyway; the two extra roundings change the outputs by far less than
+// the tolerance (checked against the oracle) and skip the unpack / repack.
+__device__ __forceinline__ void rotate_pair_bf16(U4& x, U4& y, const uint32_t (&c)[4], const uint32_t (&s)[4],
+                                                 const uint32_t (&ns)[4]) {
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+  const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+  uint32_t xo[4], yo[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    xo[k] = ptx::fma_bf2(yw[k], ns[k], ptx::mul_bf2(xw[k], c[k]));
+    yo[k] = ptx::fma_bf2(xw[k], s[k], ptx::mul_bf2(yw[k], c[k]));
+  }
+  x = U4{xo[0], xo[1], xo[2], xo[3]};
+  y = U4{yo[0], yo[1], yo[2], yo[3]};
+}
+
 __device__ __forceinline__ uint32_t w_of(const U4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
@@ -208,7 +227,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   const float qs = a.scale * kLog2e;  // applied to the scores; softmax runs in base 2
 
   // R_s for the two key rows (slots g8, g8 + 8) of this thread, as packed pairs
-  uint64_t rsc[2][GE::NPAIR][4], rss[2][GE::NPAIR][4];
+  // cos, sin and -sin of the slot angles of key rows g8 and g8 + 8, as bf16 pairs
+  uint32_t rcb[2][GE::NPAIR][4], rsb[2][GE::NPAIR][4], rnb[2][GE::NPAIR][4];
   int tq = 0;
   if constexpr (ROPE) {
 #pragma unroll
@@ -221,8 +241,9 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
         for (int e = 0; e < 4; ++e) {
           const float2 c = __ldg(reinterpret_cast<const float2*>(t + ch.fbase[p] + 2 * e));
           const float2 sn = __ldg(reinterpret_cast<const float2*>(t + D / 2 + ch.fbase[p] + 2 * e));
-          rsc[row][p][e] = ptx::f2(c.x, c.y);
-          rss[row][p][e] = ptx::f2(sn.x, sn.y);
+          rcb[row][p][e] = ptx::pack_bf16(c.x, c.y);
+          rsb[row][p][e] = ptx::pack_bf16(sn.x, sn.y);
+          rnb[row][p][e] = ptx::pack_bf16(-sn.x, -sn.y);
         }
       }
     }
@@ -368,7 +389,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
       for (int row = 0; row < 2; ++row)
 #pragma unroll
         for (int p = 0; p < GE::NPAIR; ++p)
-          rotate_pair(kr[row][ch.first[p]], kr[row][ch.second[p]], rsc[row][p], rss[row][p]);
+          rotate_pair_bf16(kr[row][ch.first[p]], kr[row][ch.second[p]], rcb[row][p], rsb[row][p], rnb[row][p]);
     }
 
     // S^T = K' Q'^T, two independent accumulation chains (even / odd k-steps)
