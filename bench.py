@@ -262,18 +262,32 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------- GPU legs
 
-def kernel_traffic(kernel_file: str, workload: str):
-    """DRAM bytes per launch from a committed ncu capture, only while the kernel
-    source is unchanged since that capture (sha256 recorded beside it)."""
+# files whose contents define the decode kernel the headline times
+DECODE_SOURCES = ("decode_mma.cu", "decode_body.cuh", "ptx.cuh")
+
+
+def kernel_sources_sha256(kernel_files) -> str:
+    """sha256 over the kernel's source files, in the order given."""
     import hashlib
+    h = hashlib.sha256()
+    for f in kernel_files:
+        h.update(open(os.path.join(ROOT, "position_independent_kv_paged_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def kernel_traffic(kernel_files, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, only while the kernel
+    sources are unchanged since that capture (sha256 recorded beside it)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    src = os.path.join(ROOT, "position_independent_kv_paged_gb300", "csrc", kernel_file)
-    if not (os.path.exists(path) and os.path.exists(src)):
+    if not os.path.exists(path):
         return None
     rec = json.load(open(path)).get(workload)
     if not rec:
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    try:
+        sha = kernel_sources_sha256(kernel_files)
+    except OSError:
+        return None
     return rec["traffic"] if rec.get("source_sha256") == sha else None
 
 
@@ -574,7 +588,7 @@ def run_minipic(args):
                            logical_kv_bytes=nbytes, unique_kv_bytes=unique_kv_bytes(w)),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                          "frac": achieved / pk["hbm"],
-                         "traffic": kernel_traffic("decode_mma.cu", "rag_decode"),
+                         "traffic": kernel_traffic(DECODE_SOURCES, "rag_decode"),
                          "peak_source": pk["src"],
                          "kernel": "decode_mma_kernel (split-KV with the cross-split merge in-kernel)",
                          "bytes": "logical K+V bytes gathered per request (sum_r L_r * Hkv * d * 2 * 2)"},
