@@ -16,9 +16,9 @@
 // Per 16-key block and GQA group (up to 8 query heads per n-tile):
 //   S^T[key][head] = K'[key][:] . Q'[head][:]  (mma m16n8k16, M = the 16 keys)
 //   O^T[dim][head] += V^T[dim][key] P^T[key][head]
-// K' is formed in registers: rows are read from shared memory, rotated in
-// fp32 with two multiply-adds per element, and packed to bf16 as the MMA's A
-// operand.  The contraction order of the head dimension is a per-thread
+// K' is formed in registers: rows are read from shared memory and rotated in
+// packed bf16 arithmetic (two bf16x2 multiply / multiply-adds per pair of
+// elements) straight into the MMA's bf16 A operand; Q' likewise.  The contraction order of the head dimension is a per-thread
 // permutation chosen so that each rotary pair (i, i + d/2) is thread-local;
 // Q' uses the same permutation.
 //
@@ -99,29 +99,12 @@ __device__ __forceinline__ uint32_t swz(int half, int key, int chunk) {
   return (uint32_t)((half * 16 + key) * 128 + ((chunk ^ (key & 7)) << 4));
 }
 
-// Rotate one pair of 8-element bf16 chunks in fp32 (packed pairs) and repack:
-//   x' = x c - y s,  y' = y c + x s   (s already carries the pair's sign)
-// c2/s2 hold the 8 cosines/sines as 4 packed fp32 pairs.
-__device__ __forceinline__ void rotate_pair(U4& x, U4& y, const uint64_t (&c2)[4], const uint64_t (&s2)[4]) {
-  uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-  uint32_t yw[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint64_t xv = ptx::bf2_to_f2(xw[k]), yv = ptx::bf2_to_f2(yw[k]);
-    const uint64_t xn = ptx::sub2(ptx::mul2(xv, c2[k]), ptx::mul2(yv, s2[k]));
-    const uint64_t yn = ptx::fma2(xv, s2[k], ptx::mul2(yv, c2[k]));
-    xw[k] = ptx::f2_to_bf2(xn);
-    yw[k] = ptx::f2_to_bf2(yn);
-  }
-  x = U4{xw[0], xw[1], xw[2], xw[3]};
-  y = U4{yw[0], yw[1], yw[2], yw[3]};
-}
-
-// The same rotation for key rows by the slot angle, in packed bf16 arithmetic:
-//   x' = bf16(y (-s) + bf16(x c)),  y' = bf16(x s + bf16(y c))
-// (c, s, -s as bf16 pairs).  The keys feed a bf16 product, so they are rounded
-// to bf16 anyway; the two extra roundings change the outputs by far less than
-// the tolerance (checked against the oracle) and skip the unpack / repack.
+// Rotate one pair of 8-element bf16 chunks (rotary halves x, y) in packed bf16
+// arithmetic: x' = bf16(y (-s) + bf16(x c)),  y' = bf16(x s + bf16(y c)), with
+// c, s, -s as bf16 pairs.  Keys and queries feed a bf16 product, so they are
+// rounded to bf16 anyway; the two extra roundings change the outputs by far
+// less than the tolerance (checked against the oracle) and skip the fp32
+// unpack / repack.
 __device__ __forceinline__ void rotate_pair_bf16(U4& x, U4& y, const uint32_t (&c)[4], const uint32_t (&s)[4],
                                                  const uint32_t (&ns)[4]) {
   const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
@@ -352,26 +335,27 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
 
     // re-rotate q by t - start from the staged table row
     if constexpr (ROPE) {
-      const float sg = delta < 0 ? -1.f : 1.f;
+      // cos and sin of |t - start| as bf16 pairs; the sign of t - start flips sin
+      const uint32_t sgn = delta < 0 ? 0x80008000u : 0u;
 #pragma unroll
       for (int p = 0; p < GE::NPAIR; ++p) {
         const U4 c0 = ptx::lds128(rowb + 4 * ch.fbase[p]);
         const U4 c1 = ptx::lds128(rowb + 4 * ch.fbase[p] + 16);
         const U4 s0 = ptx::lds128(rowb + 2 * D + 4 * ch.fbase[p]);
         const U4 s1 = ptx::lds128(rowb + 2 * D + 4 * ch.fbase[p] + 16);
-        uint64_t c2[4], s2[4];
-        c2[0] = ptx::f2(__uint_as_float(c0.x), __uint_as_float(c0.y));
-        c2[1] = ptx::f2(__uint_as_float(c0.z), __uint_as_float(c0.w));
-        c2[2] = ptx::f2(__uint_as_float(c1.x), __uint_as_float(c1.y));
-        c2[3] = ptx::f2(__uint_as_float(c1.z), __uint_as_float(c1.w));
-        s2[0] = ptx::f2(sg * __uint_as_float(s0.x), sg * __uint_as_float(s0.y));
-        s2[1] = ptx::f2(sg * __uint_as_float(s0.z), sg * __uint_as_float(s0.w));
-        s2[2] = ptx::f2(sg * __uint_as_float(s1.x), sg * __uint_as_float(s1.y));
-        s2[3] = ptx::f2(sg * __uint_as_float(s1.z), sg * __uint_as_float(s1.w));
+        const uint32_t cb[4] = {ptx::pack_bf16(__uint_as_float(c0.x), __uint_as_float(c0.y)),
+                                ptx::pack_bf16(__uint_as_float(c0.z), __uint_as_float(c0.w)),
+                                ptx::pack_bf16(__uint_as_float(c1.x), __uint_as_float(c1.y)),
+                                ptx::pack_bf16(__uint_as_float(c1.z), __uint_as_float(c1.w))};
+        const uint32_t sb[4] = {ptx::pack_bf16(__uint_as_float(s0.x), __uint_as_float(s0.y)) ^ sgn,
+                                ptx::pack_bf16(__uint_as_float(s0.z), __uint_as_float(s0.w)) ^ sgn,
+                                ptx::pack_bf16(__uint_as_float(s1.x), __uint_as_float(s1.y)) ^ sgn,
+                                ptx::pack_bf16(__uint_as_float(s1.z), __uint_as_float(s1.w)) ^ sgn};
+        const uint32_t nb[4] = {sb[0] ^ 0x80008000u, sb[1] ^ 0x80008000u, sb[2] ^ 0x80008000u, sb[3] ^ 0x80008000u};
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           U4 x = qraw[nt][ch.first[p]], y = qraw[nt][ch.second[p]];
-          rotate_pair(x, y, c2, s2);
+          rotate_pair_bf16(x, y, cb, sb, nb);
           qw[nt][ch.first[p]] = x;
           qw[nt][ch.second[p]] = y;
         }
