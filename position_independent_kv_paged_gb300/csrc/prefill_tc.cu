@@ -1,4 +1,5 @@
-// Prefill kernel wrapper and launcher (the CTA body is in prefill2_body.cuh).
+// Prefill kernel wrapper and launcher for head dim 64 (the CTA body is in
+// prefill2_body.cuh; head dim 128 goes to the CTA-pair kernel).
 #include "prefill2_body.cuh"
 #include "tmap.cuh"
 
@@ -49,10 +50,11 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Head dim 128 runs the CTA-pair kernel; head dim 64 this single-CTA kernel.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, bool rotate, cudaStream_t s) {
   if (a.D == 128) return launch_prefill_pair(a, rotate, s);
-  if (rotate) return a.D == 128 ? launch_t<128, true>(a, s) : launch_t<64, true>(a, s);
-  return a.D == 128 ? launch_t<128, false>(a, s) : launch_t<64, false>(a, s);
+  if (a.D != 64) return cudaErrorInvalidValue;
+  return rotate ? launch_t<64, true>(a, s) : launch_t<64, false>(a, s);
 }
 
 }  // namespace minipic
