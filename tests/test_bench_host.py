@@ -94,3 +94,27 @@ def test_prefill_flops_count_only_the_causal_key_set():
 def test_whole_job_value_scales_with_ranks():
     assert bench.whole_job_gbs(10**9, 1, 1.0) == pytest.approx(1000.0)
     assert bench.whole_job_gbs(10**9, 4, 2.0) == pytest.approx(2000.0)
+
+
+REF_CMD = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"]
+
+
+def test_reference_arm_prints_one_contract_line():
+    out = subprocess.run(REF_CMD, cwd=ROOT, capture_output=True, text=True, check=True, timeout=600).stdout
+    lines = [ln for ln in out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["steps"] == 1 and d["warmup"] == 0 and d["value"] > 0 and d["higher_is_better"] is True
+    cb = d["cpu_baseline"]
+    assert cb["value"] == d["value"] and cb["kind"] == "oracle" and cb["cores"] == bench.ORACLE_THREADS
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    r = subprocess.run(REF_CMD, cwd=ROOT, capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip() == ""
