@@ -33,6 +33,9 @@ __all__ = [
     "attn_prefill",
     "attn_prefill_prerotated",
     "attn_mixed",
+    "kv_append",
+    "kv_swap_out",
+    "kv_swap_in",
     "device_error",
     "STATUS",
 ]
