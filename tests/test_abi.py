@@ -33,6 +33,21 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+def test_binding_covers_the_entry_points():
+    """Every public name of the binding exists, and every call of the header has
+    a Python wrapper (the allocation-free decode is a C-only convenience and the
+    status strings live in STATUS)."""
+    for n in mp.__all__:
+        assert hasattr(mp, n), n
+    c_only = {"minipic_attn_decode_noalloc", "minipic_status_string"}
+    renamed = {"minipic_attn_decode_workspace_size": "decode_workspace_size",
+               "minipic_attn_prefill_workspace_size": "prefill_workspace_size"}
+    for n in declared_functions():
+        if n in c_only:
+            continue
+        assert renamed.get(n, n[len("minipic_"):]) in mp.__all__, n
+
+
 def test_library_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(mp.library_path())
     missing = [n for n in declared_functions() if not hasattr(raw, n)]
