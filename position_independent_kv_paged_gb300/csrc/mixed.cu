@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(kMixThreads, 1)
     const int per = P.a.Hkv * P.a.batch;
     const int pr_rev = i / per, rem = i - pr_rev * per;
     const int hk = rem / P.a.batch, r = rem - hk * P.a.batch;
-    prefill2_impl::prefill2_cta<D, true>(&kmap, &vblk, P, n_pairs - 1 - pr_rev, -1, n_pairs, hk, r, smem_raw);
+    prefill2_impl::prefill2_cta<D, true>(&kmap, &vblk, P, n_pairs - 1 - pr_rev, n_pairs, hk, r, smem_raw);
   } else {
     const int j = i - n_pre;
     const int split = j % Dd.n_split, rest = j / Dd.n_split;

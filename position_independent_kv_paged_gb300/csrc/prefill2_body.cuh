@@ -121,15 +121,13 @@ __device__ __forceinline__ void rot_pack(U4& x, U4& y, const uint64_t (&c2)[4], 
   y = U4{yw[0], yw[1], yw[2], yw[3]};
 }
 
-// MC: the CTA is one of a 2-CTA cluster whose other CTA (query-tile pair
-// peer_pair of the same request and kv head) reads the same K~/V tiles; each
-// CTA fetches the boxes of half the blocks of a tile and multicasts them to
-// both, and a stage is refilled only once both CTAs have released it.
-// vmap_p is the block view of the V pool (make_pool_block_map).
-template <int D, bool ROPE, bool MC = false, int NB = kNB, int NSK = kNSK, int NSV = kNSV>
+// One CTA computes query-tile pair `pair` of request r and kv head hk and
+// loads every K~/V box it reads itself.  vmap_p is the block view of the V pool
+// (make_pool_block_map).
+template <int D, bool ROPE, int NB = kNB, int NSK = kNSK, int NSV = kNSV>
 __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p,
-                                             const PrefillLaunch2& L, const int pair, const int peer_pair,
-                                             const int n_pairs, const int hk, const int r, uint8_t* smem_raw) {
+                                             const PrefillLaunch2& L, const int pair, const int n_pairs,
+                                             const int hk, const int r, uint8_t* smem_raw) {
   using G_ = PG2<D, NB, NSK, NSV>;
   constexpr int BN = G_::BN;
   const PrefillArgs& a = L.a;
@@ -150,7 +148,7 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
   const int tok0 = 2 * pair * TQ;  // first token of query tile 0
   if (tid == 0 && pair == n_pairs - 1 && ql > n_pairs * 2 * TQ) atomicOr(a.err, kErrSeqLen);
   auto has_rows = [&](int pr) { return pr >= 0 && ql > 0 && 2 * pr * TQ < ql; };
-  if (!has_rows(pair) && (!MC || !has_rows(peer_pair))) return;  // the same in both CTAs of a cluster
+  if (!has_rows(pair)) return;
   int kvl = a.kv_lens[r];
   if (kvl < ql || kvl > mb * 16) {
     if (tid == 0 && pair == 0) atomicOr(a.err, kErrSeqLen);
@@ -163,8 +161,7 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
     const int lim_last = kvl - ql + t0 + min(2 * TQ, ql - t0) - 1;
     return lim_last >= 0 ? lim_last / BN + 1 : 0;
   };
-  const int n_kt = tiles_of(pair);                                  // tiles this CTA computes on
-  const int n_ld = MC ? max(n_kt, tiles_of(peer_pair)) : n_kt;      // tiles this CTA helps load
+  const int n_kt = tiles_of(pair);  // key tiles this CTA loads and computes on
 
   // ------------------------------------------------------------ setup
   if (tid == 0) {
@@ -172,11 +169,11 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
     for (int s = 0; s < NSK; ++s) {
       ptx::mbar_init(bar(G_::B_KFULL + s), 1);
       ptx::mbar_init(bar(G_::B_KROT + s), kRotThreads);
-      ptx::mbar_init(bar(G_::B_KFREE + s), MC ? 2 : 1);
+      ptx::mbar_init(bar(G_::B_KFREE + s), 1);
     }
     for (int s = 0; s < NSV; ++s) {
       ptx::mbar_init(bar(G_::B_VFULL + s), 1);
-      ptx::mbar_init(bar(G_::B_VFREE + s), MC ? 2 : 1);
+      ptx::mbar_init(bar(G_::B_VFREE + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(G_::B_S + i), 1);
@@ -196,11 +193,8 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
   ptx::fence_proxy_async_smem();
   umma::fence_before_sync();
   __syncthreads();
-  if constexpr (MC) ptx::cluster_sync();  // the peer's barriers exist before anything is multicast
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const uint32_t crank = MC ? ptx::cluster_rank() : 0u;
-  constexpr uint16_t kBoth = 3;
 
   if (warp == kTmaWarp) {
     // ======================================================== TMA producer
@@ -213,11 +207,10 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
     constexpr int LAG = NSK - NSV;
     constexpr unsigned FULL = 0xffffffffu;
     static_assert(NB * G_::HALVES + NB <= 32, "one lane per copy");
-    if (n_ld > 0) {
+    if (n_kt > 0) {
       const int* bt = a.block_tables + (size_t)r * mb;
       const int* bs = a.block_starts + (size_t)r * mb;
       const int blk = lane % NB, hh = lane / NB;
-      const bool mine = !MC || (uint32_t)(blk & 1) == crank;  // with MC: blocks of this CTA's parity
       int my_ph = -1, my_st = 0;  // lanes < NB: block NB u + lane of the next K~ tile
       auto fetch = [&](int t) {
         const int b = NB * t + lane;
@@ -227,8 +220,8 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
       };
       bool ok = true;
       fetch(0);
-      for (int u = 0; u < n_ld + LAG; ++u) {
-        if (u < n_ld) {
+      for (int u = 0; u < n_kt + LAG; ++u) {
+        if (u < n_kt) {
           const int s = u % NSK;
           bool w = true;
           if (lane == 0 && u >= NSK) w = ptx::mbar_wait(bar(G_::B_KFREE + s), ((u / NSK) - 1) & 1);
@@ -236,7 +229,7 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
           int flag = 0;
           if (lane < NB && NB * u + lane < nblk) {
             if (my_ph >= 0 && my_ph < a.num_blocks) flag |= 1;
-            else if (crank == 0) atomicOr(a.err, kErrBlockId);
+            else atomicOr(a.err, kErrBlockId);
             if (!ROPE || (my_st >= 0 && my_st < a.max_pos)) flag |= 2;
           }
           int* m = meta + 3 * NB * s;
@@ -254,23 +247,17 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
             ptx::mbar_arrive_expect_tx(bar(G_::B_KFULL + s), __popc(kv) * G_::HALVES * 2048 + __popc(rw) * G_::ROWB);
           __syncwarp();
           if (lane < NB * G_::HALVES) {
-            if (mine && ((kv >> blk) & 1u)) {
+            if ((kv >> blk) & 1u) {
               const uint32_t dst = sbase + G_::OFF_K + s * G_::KTILE + hh * (BN * 128) + blk * 2048;
-              if constexpr (MC)
-                ptx::tma_load_2d_mc(dst, &kmap, 64 * hh, (ph_l * a.Hkv + hk) * 16, bar(G_::B_KFULL + s), kBoth);
-              else
-                ptx::tma_load_2d(dst, &kmap, 64 * hh, (ph_l * a.Hkv + hk) * 16, bar(G_::B_KFULL + s));
+              ptx::tma_load_2d(dst, &kmap, 64 * hh, (ph_l * a.Hkv + hk) * 16, bar(G_::B_KFULL + s));
             }
           } else if (ROPE && lane < NB * G_::HALVES + NB) {
-            if (mine && ((rw >> blk) & 1u)) {
+            if ((rw >> blk) & 1u) {
               const uint32_t dst = sbase + G_::OFF_RS + (s * NB + blk) * G_::ROWB;
-              if constexpr (MC)
-                ptx::bulk_load_mc(dst, a.cos_sin + (size_t)st_l * D, G_::ROWB, bar(G_::B_KFULL + s), kBoth);
-              else
-                ptx::bulk_load(dst, a.cos_sin + (size_t)st_l * D, G_::ROWB, bar(G_::B_KFULL + s));
+              ptx::bulk_load(dst, a.cos_sin + (size_t)st_l * D, G_::ROWB, bar(G_::B_KFULL + s));
             }
           }
-          if (u + 1 < n_ld) fetch(u + 1);
+          if (u + 1 < n_kt) fetch(u + 1);
         }
         const int tv = u - LAG;
         if (tv >= 0) {
@@ -283,12 +270,9 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
           const unsigned vv = __ballot_sync(FULL, lane < NB && ph >= 0);
           if (lane == 0) ptx::mbar_arrive_expect_tx(bar(G_::B_VFULL + sv), __popc(vv) * G_::HALVES * 2048);
           __syncwarp();
-          if (lane < NB && ph >= 0 && mine) {  // one box per block: [half][16 rows][64]
+          if (lane < NB && ph >= 0) {  // one box per block: [half][16 rows][64]
             const uint32_t dst = sbase + G_::OFF_V + sv * G_::KTILE + blk * (G_::HALVES * 2048);
-            if constexpr (MC)
-              ptx::tma_load_3d_mc(dst, &vmap, 0, (ph * a.Hkv + hk) * 16, 0, bar(G_::B_VFULL + sv), kBoth);
-            else
-              ptx::tma_load_3d(dst, &vmap, 0, (ph * a.Hkv + hk) * 16, 0, bar(G_::B_VFULL + sv));
+            ptx::tma_load_3d(dst, &vmap, 0, (ph * a.Hkv + hk) * 16, 0, bar(G_::B_VFULL + sv));
           }
         }
       }
@@ -297,17 +281,10 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ======================================================== MMA issue
-    if (lane == 0 && n_ld > 0) {
-      // release a K~ / V stage: to both CTAs with MC, and there only while some
-      // later tile of the cluster still refills it (so no arrival outlives a peer)
-      auto free_k = [&](int u) {
-        if (!MC) umma::commit(bar(G_::B_KFREE + u % NSK));
-        else if (u + NSK < n_ld) umma::commit_mc(bar(G_::B_KFREE + u % NSK), kBoth);
-      };
-      auto free_v = [&](int u) {
-        if (!MC) umma::commit(bar(G_::B_VFREE + u % NSV));
-        else if (u + NSV < n_ld) umma::commit_mc(bar(G_::B_VFREE + u % NSV), kBoth);
-      };
+    if (lane == 0 && n_kt > 0) {
+      // release a K~ / V stage once the products that read it are done
+      auto free_k = [&](int u) { umma::commit(bar(G_::B_KFREE + u % NSK)); };
+      auto free_v = [&](int u) { umma::commit(bar(G_::B_VFREE + u % NSV)); };
       const uint32_t id_qk = ROPE ? umma::idesc_f16_f32(128, BN, false, false)
                                   : umma::idesc_bf16_f32(128, BN, false, false);
       const uint32_t id_pv = umma::idesc_bf16_f32(128, D, false, true);
@@ -363,22 +340,6 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
           }
         }
         umma::commit(bar(G_::B_ODONE));
-      }
-      // tiles loaded only for the cluster peer: wait for them to land, then release
-      for (int u = n_kt; MC && ok && u < n_ld; ++u) {
-        if (!ptx::mbar_wait(bar(G_::B_KFULL + u % NSK), (u / NSK) & 1) ||
-            !ptx::mbar_wait(bar(G_::B_VFULL + u % NSV), (u / NSV) & 1)) {
-          ok = false;
-          break;
-        }
-        if (u + NSK < n_ld) {
-          ptx::mbar_arrive_remote(bar(G_::B_KFREE + u % NSK), 0);
-          ptx::mbar_arrive_remote(bar(G_::B_KFREE + u % NSK), 1);
-        }
-        if (u + NSV < n_ld) {
-          ptx::mbar_arrive_remote(bar(G_::B_VFREE + u % NSV), 0);
-          ptx::mbar_arrive_remote(bar(G_::B_VFREE + u % NSV), 1);
-        }
       }
       if (!ok) atomicOr(a.err, kErrTimeout);
     }
@@ -684,7 +645,6 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
   umma::fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) umma::tmem_dealloc(tmem, G_::TCOLS);
-  if constexpr (MC) ptx::cluster_sync();  // no CTA leaves while its peer may still write to it
 }
 
 }  // namespace prefill2_impl

@@ -8,8 +8,8 @@ namespace {
 
 using namespace prefill2_impl;
 
-// Launched in clusters of two along x: CTAs 2c and 2c + 1 (adjacent query-tile
-// pairs of one request and kv head) share every K~/V tile through multicast.
+// One CTA per (query-tile pair, kv head, request); each CTA loads its own K~/V
+// tiles.
 template <int D, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -17,8 +17,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   // heaviest (latest) query-tile pairs first
   const int n = gridDim.x;
-  prefill2_cta<D, ROPE, true>(&kmap, &vmap, L, n - 1 - (int)blockIdx.x, n - 1 - (int)(blockIdx.x ^ 1u), n,
-                              blockIdx.y, blockIdx.z, smem_raw);
+  prefill2_cta<D, ROPE>(&kmap, &vmap, L, n - 1 - (int)blockIdx.x, n, blockIdx.y, blockIdx.z, smem_raw);
 }
 
 template <int D, bool ROPE>
@@ -33,19 +32,10 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   PrefillLaunch2 L{a, 128 / a.G};
   const int n_pairs = (a.max_q_len + 2 * L.tq - 1) / (2 * L.tq);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((n_pairs + 1) & ~1), (unsigned)a.Hkv, (unsigned)a.batch);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, ROPE>, km, vm, L);
+  if (n_pairs <= 0) return cudaSuccess;
+  prefill_tc_kernel<D, ROPE>
+      <<<dim3((unsigned)n_pairs, (unsigned)a.Hkv, (unsigned)a.batch), kThreads, smem, s>>>(km, vm, L);
+  return cudaGetLastError();
 }
 
 }  // namespace

@@ -83,15 +83,6 @@ __device__ __forceinline__ void commit(uint32_t mbar) {
                : "memory");
 }
 
-// Arrive on the mbarrier at the same shared offset of every CTA in cta_mask once
-// all previously issued tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void commit_mc(uint32_t mbar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(mbar),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- TMEM <-> registers
 // 32x32b shape: thread t of the warp reads TMEM lane (lane base + t), N consecutive columns.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
