@@ -32,7 +32,6 @@ from .attention import (
     widen,
     key_index_map,
     attend,
-    decode_head,
     decode,
     prefill_request,
     prefill,
@@ -47,7 +46,6 @@ __all__ = [
     "widen",
     "key_index_map",
     "attend",
-    "decode_head",
     "decode",
     "prefill_request",
     "prefill",

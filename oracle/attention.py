@@ -85,20 +85,6 @@ def _gathered(w, table_row, start_row, n_keys, g):
     return k, v, pos
 
 
-def decode_head(w, r: int, h: int, scale: float = 0.0):
-    """Decode output (out [d], lse) of request r, query head h."""
-    dec = w.decode
-    G = w.Hq // w.Hkv
-    g = h // G
-    n = int(dec.seq_lens[r])
-    k, v, pos = _gathered(w, dec.block_tables[r], dec.block_starts[r], n, g)
-    q = widen(dec.q[r, h][None, :], w.dtype)
-    qr = rope_rotate(q, [int(dec.q_pos[r])], w.rope_base)
-    kr = rope_rotate(k, pos, w.rope_base)
-    o, l = attend(qr, kr, v, _scale(w, scale))
-    return o[0], l[0]
-
-
 def decode(w, requests: Optional[Iterable[int]] = None, scale: float = 0.0):
     """Decode outputs for the requested requests (all by default).
 

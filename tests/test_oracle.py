@@ -472,11 +472,12 @@ def test_pins_catch_wrong_gqa_mapping(monkeypatch):
         for r in range(dec.batch):
             for h in range(w.Hq):
                 # wrong: head h reads kv head h % Hkv instead of h // G
-                w2 = W.Workload(w.name, w.dtype, w.Hkv, w.Hkv, w.d, w.block_size, w.rope_base, w.max_pos, w.kv)
-                w2.decode = W.DecodeBatch(dec.q[r:r + 1, [h] * w.Hkv], dec.block_tables[r:r + 1],
-                                          dec.block_starts[r:r + 1], dec.seq_lens[r:r + 1], dec.q_pos[r:r + 1])
-                o, l = oatt.decode_head(w2, 0, h % w.Hkv)
-                out[r, h], lse[r, h] = o, l
+                k, v, pos = oatt._gathered(w, dec.block_tables[r], dec.block_starts[r], int(dec.seq_lens[r]),
+                                           h % w.Hkv)
+                qr = oracle.rope_rotate(oracle.widen(dec.q[r, h][None, :], w.dtype), [int(dec.q_pos[r])],
+                                        w.rope_base)
+                o, l = oracle.attend(qr, oracle.rope_rotate(k, pos, w.rope_base), v, 1.0 / np.sqrt(w.d))
+                out[r, h], lse[r, h] = o[0], l[0]
         return out, lse
     w = W.tiny_decode(0, "f32")
     bo, _ = brute_decode(w)
