@@ -30,7 +30,9 @@
  *  - Queries are passed unrotated with their positions; the kernels rotate them.
  *  - The rotary table is the device array written by minipic_rope_table:
  *    float [max_pos][head_dim], cos(p theta_i) in columns [0, d/2) and
- *    sin(p theta_i) in columns [d/2, d).  Every position used must be < max_pos.
+ *    sin(p theta_i) in columns [d/2, d), plus (for the prefill and mixed calls)
+ *    the same values rounded to fp16 in a second array of that layout, written
+ *    by minipic_rope_table_f16.  Every position used must be < max_pos.
  *  - scale <= 0 selects 1/sqrt(head_dim).
  *  - Outputs: out has the layout of q and the call's dtype; lse (optional, may
  *    be NULL) is float, natural-log log-sum-exp of the scaled scores per
@@ -87,6 +89,9 @@ typedef enum { MINIPIC_F32 = 0, MINIPIC_BF16 = 1 } minipic_dtype;
 #define MINIPIC_DEVERR_POSITION   2  /* a key or query position outside [0, max_pos) */
 #define MINIPIC_DEVERR_SEQ_LEN    4  /* a length above max_blocks_per_seq * block_size or negative */
 #define MINIPIC_DEVERR_TIMEOUT    8  /* a bounded wait for an asynchronous copy gave up (results invalid) */
+#define MINIPIC_DEVERR_RANGE     16  /* prefill: a rotated key or scaled, rotated query element is outside the
+                                        fp16 range of the QK^T operands (|x| > 65504); the score rows that
+                                        use it are undefined (inf or NaN), all other rows are unaffected */
 
 /* The paged KV pool (device memory, caller-owned). */
 typedef struct {
@@ -98,11 +103,15 @@ typedef struct {
   int32_t head_dim;       /* 64 or 128 */
 } minipic_kv_pool;
 
-/* The rotary cos/sin table written by minipic_rope_table (device memory). */
+/* The rotary cos/sin table (device memory, caller-owned). */
 typedef struct {
-  const float* cos_sin;   /* [max_pos][head_dim] */
+  const float* cos_sin;          /* [max_pos][head_dim] fp32, written by minipic_rope_table */
   int32_t max_pos;
-  int32_t head_dim;       /* must equal the pool's head_dim */
+  int32_t head_dim;              /* must equal the pool's head_dim */
+  const uint16_t* cos_sin_f16;   /* [max_pos][head_dim] fp16 bit patterns, written by
+                                    minipic_rope_table_f16 with the same max_pos, head_dim
+                                    and base; read by the prefill and mixed calls (NULL
+                                    there returns INVALID), ignored by decode (may be NULL) */
 } minipic_rope;
 
 /* One decode token per request (MiniPIC section 2.1 score equation with the
@@ -150,6 +159,18 @@ const char* minipic_status_string(minipic_status status);
  * rope_base <= 0; CUDA on launch failure. */
 minipic_status minipic_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim,
                                   double rope_base, minipic_stream_t stream);
+
+/* The same table rounded to fp16 (MiniPIC section 2.1, the cosine/sine table
+ * the key rotation reads): cos_sin_f16[p*head_dim + i] and [p*head_dim + d/2 + i]
+ * hold cos and sin of p theta_i, formed in double precision and rounded once to
+ * the nearest fp16 (IEEE binary16 bit patterns; values below 2^-14 become
+ * subnormals, whose absolute error is at most 2^-25).  The chunked-prefill
+ * kernels rotate keys with it in packed fp16 arithmetic, sixteen consecutive
+ * positions of a block being sixteen consecutive rows.  cos_sin_f16: device,
+ * at least max_pos * head_dim uint16 values, 16-byte aligned, caller-owned.
+ * Errors as for minipic_rope_table. */
+minipic_status minipic_rope_table_f16(uint16_t* cos_sin_f16, int32_t max_pos, int32_t head_dim,
+                                      double rope_base, minipic_stream_t stream);
 
 /* Workspace bytes minipic_attn_decode needs for this shape on the current
  * device (split-KV partial results).  0 means no workspace is needed.  The
@@ -223,11 +244,14 @@ size_t minipic_attn_prefill_workspace_size(int32_t batch, int32_t num_q_heads, i
 /* Chunked prefill over cached span blocks plus the chunk's own keys (the
  * uncached-span prefill of MiniPIC section 4 and the final-prompt prefill that
  * reads cached spans).  Keys are rotated at pi(j) into shared memory and the
- * products run on the tcgen05 tensor cores with TMEM accumulators.  The
- * rotated q and k are rounded to fp16 for the QK^T product (10-bit mantissa:
- * rotated elements must stay within +-65504); softmax weights and V are bf16
- * for the P.V product; accumulation is fp32.  bf16 only (f32 returns
- * UNSUPPORTED).  The workspace is not used (size 0).  Errors as for decode. */
+ * products run on the tcgen05 tensor cores with TMEM accumulators.  Keys are
+ * rotated in packed fp16 arithmetic with the fp16 table (rope->cos_sin_f16,
+ * required); the query is rotated in fp32 with the fp32 table.  The rotated q
+ * and k are fp16 for the QK^T product (10-bit mantissa: rotated elements must
+ * stay within +-65504; an element outside sets MINIPIC_DEVERR_RANGE and the
+ * rows that read it are undefined); softmax weights and V are bf16 for the P.V product;
+ * accumulation is fp32.  bf16 only (f32 returns UNSUPPORTED).  The workspace
+ * is not used (size 0).  Errors as for decode. */
 minipic_status minipic_attn_prefill(minipic_dtype dtype, int32_t num_q_heads,
                                     const minipic_kv_pool* kv, const minipic_rope* rope,
                                     const minipic_prefill_batch* batch, float scale,

@@ -25,7 +25,9 @@ __all__ = [
     "MiniPICError",
     "library_path",
     "load",
+    "RopeTable",
     "rope_table",
+    "rope_table_f16",
     "decode_workspace_size",
     "attn_decode",
     "attn_decode_prerotated",
@@ -68,7 +70,8 @@ class _Append(ctypes.Structure):
 
 
 class _Rope(ctypes.Structure):
-    _fields_ = [("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+    _fields_ = [("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("cos_sin_f16", ctypes.c_void_p)]
 
 
 class _Decode(ctypes.Structure):
@@ -111,6 +114,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         L.minipic_status_string.argtypes = [ctypes.c_int]
         L.minipic_rope_table.restype = ctypes.c_int
         L.minipic_rope_table.argtypes = [c_vp, c_i32, c_i32, c_d, c_vp]
+        L.minipic_rope_table_f16.restype = ctypes.c_int
+        L.minipic_rope_table_f16.argtypes = [c_vp, c_i32, c_i32, c_d, c_vp]
         L.minipic_attn_decode_workspace_size.restype = c_sz
         L.minipic_attn_decode_workspace_size.argtypes = [c_i32] * 6
         L.minipic_attn_decode.restype = ctypes.c_int
@@ -197,17 +202,60 @@ def _kv(k_pool, v_pool) -> _KV:
 
 # ---------------------------------------------------------------- API
 
-def rope_table(max_pos: int, head_dim: int, base: float, device=None, stream=None, out=None):
-    """Build the fp32 cos/sin table [max_pos, head_dim] on the GPU."""
+class RopeTable:
+    """The rotary cos/sin table in the two forms the kernels read: ``cos_sin``
+    (float32 [max_pos, head_dim]: decode, and the prefill's query rotation) and
+    ``cos_sin_f16`` (the same values rounded to float16: the prefill's key
+    rotation).  Built by ``rope_table``."""
+
+    def __init__(self, cos_sin, cos_sin_f16=None):
+        self.cos_sin = cos_sin
+        self.cos_sin_f16 = cos_sin_f16
+
+    @property
+    def max_pos(self) -> int:
+        return int(self.cos_sin.shape[0])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.cos_sin.shape[1])
+
+
+def rope_table_f16(max_pos: int, head_dim: int, base: float, device=None, stream=None, out=None):
+    """Build the float16 cos/sin table [max_pos, head_dim] on the GPU."""
     torch = _torch()
     L = load()
     if out is None:
-        out = torch.empty((max_pos, head_dim), dtype=torch.float32,
+        out = torch.empty((max_pos, head_dim), dtype=torch.float16,
                           device=device if device is not None else "cuda")
-    _need(out, "out", dtype=torch.float32, ndim=2)
-    _check(L.minipic_rope_table(out.data_ptr(), int(max_pos), int(head_dim), float(base), _stream(stream)),
-           "minipic_rope_table")
+    _need(out, "out", dtype=torch.float16, ndim=2)
+    _check(L.minipic_rope_table_f16(out.data_ptr(), int(max_pos), int(head_dim), float(base), _stream(stream)),
+           "minipic_rope_table_f16")
     return out
+
+
+def rope_table(max_pos: int, head_dim: int, base: float, device=None, stream=None) -> RopeTable:
+    """Build the cos/sin table (float32 and float16 forms) on the GPU."""
+    torch = _torch()
+    L = load()
+    f32 = torch.empty((max_pos, head_dim), dtype=torch.float32, device=device if device is not None else "cuda")
+    _check(L.minipic_rope_table(f32.data_ptr(), int(max_pos), int(head_dim), float(base), _stream(stream)),
+           "minipic_rope_table")
+    return RopeTable(f32, rope_table_f16(max_pos, head_dim, base, device=f32.device, stream=stream))
+
+
+def _rope_struct(rope, need_f16: bool) -> _Rope:
+    """ABI view of a RopeTable (or, for decode, of a bare float32 table)."""
+    torch = _torch()
+    f32, f16 = (rope.cos_sin, rope.cos_sin_f16) if isinstance(rope, RopeTable) else (rope, None)
+    _need(f32, "rope", dtype=torch.float32, ndim=2)
+    if f16 is not None:
+        _need(f16, "rope f16", dtype=torch.float16, ndim=2)
+        if tuple(f16.shape) != tuple(f32.shape):
+            raise ValueError("the float16 and float32 tables differ in shape")
+    elif need_f16:
+        raise TypeError("prefill needs the RopeTable built by rope_table() (it carries the float16 table)")
+    return _Rope(f32.data_ptr(), f32.shape[0], f32.shape[1], None if f16 is None else f16.data_ptr())
 
 
 def decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
@@ -246,8 +294,7 @@ def _decode(q, k_pool, v_pool, block_tables, block_starts, seq_lens, q_pos, rope
                                               float(scale), ws_ptr, ws_n, _stream(stream))
         _check(st, "minipic_attn_decode_prerotated")
     else:
-        _need(rope, "rope", dtype=torch.float32, ndim=2)
-        rp = _Rope(rope.data_ptr(), rope.shape[0], rope.shape[1])
+        rp = _rope_struct(rope, False)
         st = L.minipic_attn_decode(_dtype_code(q), Hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(db),
                                    float(scale), ws_ptr, ws_n, _stream(stream))
         _check(st, "minipic_attn_decode")
@@ -302,11 +349,10 @@ def _prefill(q, cu_q_lens, q_pos, k_pool, v_pool, block_tables, block_starts, kv
                                                float(scale), _stream(stream))
         _check(st, "minipic_attn_prefill_prerotated")
         return out, lse
-    _need(rope, "rope", dtype=torch.float32, ndim=2)
+    rp = _rope_struct(rope, True)
     if workspace is None:
         n = prefill_workspace_size(B, Hq, kv.num_kv_heads, d, max_q_len, mb, kv.block_size)
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
-    rp = _Rope(rope.data_ptr(), rope.shape[0], rope.shape[1])
     st = L.minipic_attn_prefill(_dtype_code(q), Hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(pb),
                                 float(scale), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), _stream(stream))
@@ -339,7 +385,7 @@ def attn_mixed(prefill: dict, decode: dict, k_pool, v_pool, rope, scale: float =
     torch = _torch()
     L = load()
     kv = _kv(k_pool, v_pool)
-    _need(rope, "rope", dtype=torch.float32, ndim=2)
+    rp = _rope_struct(rope, True)
     pq, dq = prefill["q"], decode["q"]
     _need(pq, "prefill q", dtype=k_pool.dtype, ndim=3)
     _need(dq, "decode q", dtype=k_pool.dtype, ndim=3)
@@ -365,7 +411,6 @@ def attn_mixed(prefill: dict, decode: dict, k_pool, v_pool, rope, scale: float =
         n = decode_workspace_size(dq.shape[0], Hq, kv.num_kv_heads, kv.head_dim, decode["block_tables"].shape[1],
                                   kv.block_size)
         workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=dq.device)
-    rp = _Rope(rope.data_ptr(), rope.shape[0], rope.shape[1])
     st = L.minipic_attn_mixed(_dtype_code(pq), Hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(pb),
                               ctypes.byref(db), float(scale), workspace.data_ptr(),
                               workspace.numel() * workspace.element_size(), _stream(stream))

@@ -176,6 +176,7 @@ minipic_status build_prefill(minipic_dtype dtype, int32_t num_q_heads, const min
     if (st != MINIPIC_OK) return st;
   }
   if (dtype != MINIPIC_BF16) return MINIPIC_ERR_UNSUPPORTED;
+  if (rotate && (!rope->cos_sin_f16 || !aligned16(rope->cos_sin_f16))) return MINIPIC_ERR_INVALID;
   if (b->batch < 0 || b->total_q < 0 || b->max_q_len < 0 || b->max_blocks_per_seq < 0) return MINIPIC_ERR_INVALID;
   if (b->batch == 0 || b->total_q == 0) {
     *empty = true;
@@ -198,6 +199,7 @@ minipic_status build_prefill(minipic_dtype dtype, int32_t num_q_heads, const min
   a.block_starts = b->block_starts;
   a.kv_lens = b->kv_lens;
   a.cos_sin = rotate ? rope->cos_sin : nullptr;
+  a.cos_sin16 = rotate ? rope->cos_sin_f16 : nullptr;
   a.max_pos = rotate ? rope->max_pos : 0;
   a.out = b->out;
   a.lse = b->lse;
@@ -305,6 +307,15 @@ minipic_status minipic_rope_table(float* cos_sin, int32_t max_pos, int32_t head_
     return MINIPIC_ERR_INVALID;
   if (!(rope_base > 0.0) || !isfinite(rope_base)) return MINIPIC_ERR_INVALID;
   cudaError_t e = launch_rope_table(cos_sin, max_pos, head_dim, rope_base, (cudaStream_t)stream);
+  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
+minipic_status minipic_rope_table_f16(uint16_t* cos_sin_f16, int32_t max_pos, int32_t head_dim, double rope_base,
+                                      minipic_stream_t stream) {
+  if (!cos_sin_f16 || !aligned16(cos_sin_f16) || max_pos <= 0 || head_dim <= 0 || (head_dim & 1))
+    return MINIPIC_ERR_INVALID;
+  if (!(rope_base > 0.0) || !isfinite(rope_base)) return MINIPIC_ERR_INVALID;
+  cudaError_t e = launch_rope_table_f16(cos_sin_f16, max_pos, head_dim, rope_base, (cudaStream_t)stream);
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 

@@ -39,7 +39,8 @@ struct PrefillArgs {
   const int32_t* block_tables;
   const int32_t* block_starts;
   const int32_t* kv_lens;
-  const float* cos_sin;
+  const float* cos_sin;       // [max_pos][D] fp32 (query rotation)
+  const uint16_t* cos_sin16;  // [max_pos][D] fp16 (key rotation in the CTA-pair kernel)
   int max_pos;
   void* out;
   float* lse;
@@ -49,10 +50,11 @@ struct PrefillArgs {
 };
 
 // Error bits (mirror MINIPIC_DEVERR_* of the public header).
-enum : int { kErrBlockId = 1, kErrPosition = 2, kErrSeqLen = 4, kErrTimeout = 8 };
+enum : int { kErrBlockId = 1, kErrPosition = 2, kErrSeqLen = 4, kErrTimeout = 8, kErrRange = 16 };
 
 // Launchers; return cudaSuccess or the launch error.
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, int head_dim, double base, cudaStream_t s);
+cudaError_t launch_rope_table_f16(uint16_t* cos_sin, int max_pos, int head_dim, double base, cudaStream_t s);
 
 // Split planning of the decode kernels (same plan used for workspace sizing).
 struct DecodePlan {

@@ -391,6 +391,11 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
           s2[2] = ptx::f2(sb.x * qs, sb.y * qs); s2[3] = ptx::f2(sb.z * qs, sb.w * qs);
           rot_pack(qc[c], qc[c + D / 16], c2, s2);
         }
+        uint32_t wq = 0u;  // fp16 range watch over the rotated, scaled query
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c)
+          wq = ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(wq, qc[c].x), qc[c].y), qc[c].z), qc[c].w);
+        if (row_ok && wq != 0u) atomicOr(a.err, kErrRange);
       } else {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -439,6 +444,7 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
       if constexpr (ROPE) {
         // loads for every key first (stage and start rows are always addressable),
         // stores only for valid keys: no branch between keys, so their loads overlap
+        uint32_t wk = 0u;  // fp16 range watch over the stored keys
 #pragma unroll
         for (int b = 0; b < G_::BPG; ++b) {
           const int blk = bg * G_::BPG + b;
@@ -471,9 +477,12 @@ __device__ __forceinline__ void prefill2_cta(const CUtensorMap* kmap_p, const CU
             if (v) {
               *px = x;
               *py = y;
+              wk = ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(wk, x.x), x.y), x.z), x.w);
+              wk = ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(wk, y.x), y.y), y.z), y.w);
             }
           }
         }
+        if (wk != 0u) atomicOr(a.err, kErrRange);
       }
       // key-valid bits: warp rw covers blocks rw, rw + 6, ...; lane = slot
 #pragma unroll

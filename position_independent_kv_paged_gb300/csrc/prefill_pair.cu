@@ -29,9 +29,11 @@
 //               and keys 80 (w / 4) .. +79 of the tile; the two warps of a
 //               lane quarter combine their row maxima through shared memory;
 //               warps 0-3 first write the rotated, scaled query tile to TMEM
-//   warps 8-11  rotation of this CTA's 80 keys of every staged tile
-//   warp 12     K~ producer: this CTA's K~ blocks and block-start cos/sin
-//               rows by TMA, and the tile's key masks and V block ids
+//   warps 8-11  rotation of this CTA's 80 keys of every staged tile in
+//               packed fp16 arithmetic, each thread reading the fp16 cos|sin
+//               values of its keys' positions from the (L2-resident) table
+//   warp 12     K~ producer: this CTA's K~ blocks by TMA, and the tile's key
+//               masks, V block ids and block starts
 //   warp 13     TMEM allocation; in CTA 0 the MMA issue, in CTA 1 a relay
 //               that tells CTA 0 when its rotated keys are ready (one
 //               cluster-scope release per tile, covering what it observed)
@@ -62,7 +64,7 @@ constexpr int BH = 16 * kHalfBlocks;           // 80 keys per CTA
 constexpr int kMaskRing = 8;
 constexpr int kThreads = 15 * 32;
 constexpr int kSoftWarps = 8;
-constexpr int kRotBase = 256, kRotThreads = 128;
+constexpr int kRotBase = 256;  // first thread of the four rotation warps
 constexpr int kTmaWarp = 12, kMmaWarp = 13, kVWarp = 14;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -79,12 +81,10 @@ struct PP {
   static_assert(NSK >= NSV && NSV >= 2 && kMaskRing >= NSK + 2, "stage plan");
   static constexpr int KTILE = 2 * BH * 128;          // [half][80 keys][64] per CTA
   static constexpr int VTILE = kTileBlocks * 2048;    // [block][16 keys][64 dims of this CTA]
-  static constexpr int ROWB = 4 * D;                  // one cos|sin row
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NSK * KTILE;
-  static constexpr int OFF_RS = OFF_V + NSV * VTILE;  // [NSK][5] block-start rows
   static constexpr int META = 2 * kHalfBlocks;                 // start[5], flag[5]
-  static constexpr int OFF_META = OFF_RS + NSK * kHalfBlocks * ROWB;
+  static constexpr int OFF_META = OFF_V + NSV * VTILE;
   static constexpr int OFF_VBLK = OFF_META + NSK * META * 4;       // [ring][10] int V block ids
   static constexpr int OFF_MASK = OFF_VBLK + kMaskRing * kTileBlocks * 4;  // [ring][10] uint16
   static constexpr int OFF_RED = (OFF_MASK + kMaskRing * kTileBlocks * 2 + 15) / 16 * 16;  // [2][2][128] f32
@@ -98,7 +98,7 @@ struct PP {
   static constexpr int OFF_BAR = (OFF_FLAG + 2 * 2 * 4 * 4 + 15) / 16 * 16;
   static constexpr int OFF_TSLOT = OFF_BAR + NBARS * 8;
   static constexpr int TOTAL = OFF_TSLOT + 16;
-  static_assert(KTILE % 1024 == 0 && VTILE % 1024 == 0 && (OFF_RS % 16) == 0, "alignment");
+  static_assert(KTILE % 1024 == 0 && VTILE % 1024 == 0 && (OFF_META % 16) == 0, "alignment");
   static_assert(TOTAL + 1024 <= 232448, "shared memory");
 };
 
@@ -109,6 +109,23 @@ struct PairLaunch {
   int tq;       // tokens per 128-row query tile (= 128 / G)
   int n_pairs;  // query-tile pairs per (request, kv head)
 };
+
+// x' = x c - y s, y' = x s + y c on 8 + 8 elements: bf16 keys converted to fp16
+// (exact for |x| < 65504 down to 2^-14, then rounded to fp16 subnormals), fp16
+// cos/sin, packed fp16 multiply and multiply-add, fp16 result (the QK^T operand)
+__device__ __forceinline__ void rot_pack16(U4& x, U4& y, const U4& c, const U4& sn) {
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w}, sw[4] = {sn.x, sn.y, sn.z, sn.w};
+  uint32_t xo[4], yo[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t xh = ptx::f2_to_h2(ptx::bf2_to_f2(xw[k])), yh = ptx::f2_to_h2(ptx::bf2_to_f2(yw[k]));
+    xo[k] = ptx::fma_h2(xh, cw[k], ptx::mul_h2(yh, sw[k]) ^ 0x80008000u);
+    yo[k] = ptx::fma_h2(xh, sw[k], ptx::mul_h2(yh, cw[k]));
+  }
+  x = U4{xo[0], xo[1], xo[2], xo[3]};
+  y = U4{yo[0], yo[1], yo[2], yo[3]};
+}
 
 __device__ __forceinline__ uint32_t swz(int key, int chunk) {
   return (uint32_t)(key * 128 + ((chunk ^ (key & 7)) << 4));
@@ -171,21 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tok0 = (2 * pair + (int)crank) * TQ;  // first token of this CTA's query tile
   if (tid == 0 && crank == 0 && pair == L.n_pairs - 1 && ql > L.n_pairs * 2 * TQ) atomicOr(a.err, kErrSeqLen);
 
-  // Loads whose latency the setup below hides: the rotation warps' cos/sin of
-  // the slot angles, warps 0-3's query row and its position, and the K~
-  // producer's table entries of the first tile.
-  uint64_t rsc[4], rss[4];
-  if (ROPE && tid >= kRotBase && tid < kRotBase + kRotThreads) {
-    const int fg = (tid - kRotBase) & 7, sl = (tid - kRotBase) >> 3;
-    const float* tr = a.cos_sin + (size_t)min(sl, a.max_pos - 1) * D;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 c = __ldg(reinterpret_cast<const float2*>(tr + 8 * fg + 2 * e));
-      const float2 sn = __ldg(reinterpret_cast<const float2*>(tr + D / 2 + 8 * fg + 2 * e));
-      rsc[e] = ptx::f2(c.x, c.y);
-      rss[e] = ptx::f2(sn.x, sn.y);
-    }
-  }
+  // Loads whose latency the setup below hides: warps 0-3's query row and its
+  // position, and the K~ producer's table entries of the first tile.
   U4 qc[D / 8];
   int qpos = 0;
   if (tid < 128) {  // query row tid of this CTA's tile
@@ -315,23 +319,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane < kTileBlocks) vblk[(u % kMaskRing) * kTileBlocks + lane] = (flag & 1) ? my_ph : -1;
           const unsigned kv = __ballot_sync(FULL, mine && (flag & 1));
-          const unsigned rw = __ballot_sync(FULL, ROPE && mine && (flag & 3) == 3);
           const int ph_l = __shfl_sync(FULL, my_ph, src);
-          const int st_l = __shfl_sync(FULL, my_st, src);
           __syncwarp();
           if (lane == 0) {
             ptx::mbar_arrive(bar(P_::B_MASK + u % kMaskRing));
-            ptx::mbar_arrive_expect_tx(bar(P_::B_KFULL + s), __popc(kv) * 2 * 2048 + __popc(rw) * P_::ROWB);
+            ptx::mbar_arrive_expect_tx(bar(P_::B_KFULL + s), __popc(kv) * 2 * 2048);
           }
           __syncwarp();
           if (lane < 2 * kHalfBlocks) {
             if ((kv >> src) & 1u)
               ptx::tma_load_2d(sbase + P_::OFF_K + s * P_::KTILE + hh * (BH * 128) + kb * 2048, &kmap, 64 * hh,
                                (ph_l * a.Hkv + hk) * 16, bar(P_::B_KFULL + s));
-          } else if (ROPE && lane < 3 * kHalfBlocks) {
-            if ((rw >> src) & 1u)
-              ptx::bulk_load(sbase + P_::OFF_RS + (s * kHalfBlocks + kb) * P_::ROWB, a.cos_sin + (size_t)st_l * D,
-                             P_::ROWB, bar(P_::B_KFULL + s));
           }
           if (u + 1 < n_kt) fetch(u + 1);
         }
@@ -433,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================================================== key rotation
     const int rt = tid - kRotBase;  // 0..127
     // ---- key rotation: thread -> (frequency group fg of 8, slot sl): slot sl
-    // of this CTA's five blocks; cos/sin(sl theta_f), f = 8 fg .. 8 fg + 7, stay
-    // in registers and the block start's come from the staged table rows
-    const int fg = rt & 7, sl = rt >> 3;  // rsc / rss: loaded before the setup
+    // of this CTA's five blocks; cos/sin((start + sl) theta_f), f = 8 fg ..
+    // 8 fg + 7, are one 16-byte load each from row start + sl of the fp16 table
+    const int fg = rt & 7, sl = rt >> 3;
     const int key0 = (int)crank * BH;  // this CTA's first key of a tile
     for (int t = 0; t < n_kt; ++t) {
       const int s = t % NSK;
@@ -446,38 +444,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (ROPE) {
         const int* m = meta + P_::META * s;
         uint8_t* sk = sg + P_::OFF_K + s * P_::KTILE;
-        // every load first (stage and start rows are always addressable), stores
-        // only for valid keys: no branch between blocks, so their loads overlap
+        // every load first (an unusable key reads table row 0), stores only for
+        // valid keys: no branch between blocks, so their loads overlap
+        U4 cvs[kHalfBlocks], svs[kHalfBlocks];
+        bool vs[kHalfBlocks];
 #pragma unroll
         for (int blk = 0; blk < kHalfBlocks; ++blk) {
           const int flag = m[kHalfBlocks + blk];
           const int start = m[blk];
-          const uint8_t* rb = sg + P_::OFF_RS + (s * kHalfBlocks + blk) * P_::ROWB;
-          const U4 c0 = *reinterpret_cast<const U4*>(rb + 32 * fg);
-          const U4 c1 = *reinterpret_cast<const U4*>(rb + 32 * fg + 16);
-          const U4 s0 = *reinterpret_cast<const U4*>(rb + 2 * D + 32 * fg);
-          const U4 s1 = *reinterpret_cast<const U4*>(rb + 2 * D + 32 * fg + 16);
-          const uint64_t ac[4] = {((uint64_t)c0.y << 32) | c0.x, ((uint64_t)c0.w << 32) | c0.z,
-                                  ((uint64_t)c1.y << 32) | c1.x, ((uint64_t)c1.w << 32) | c1.z};
-          const uint64_t as[4] = {((uint64_t)s0.y << 32) | s0.x, ((uint64_t)s0.w << 32) | s0.z,
-                                  ((uint64_t)s1.y << 32) | s1.x, ((uint64_t)s1.w << 32) | s1.z};
           const int key = blk * 16 + sl;
-          const bool v = (flag & 3) == 3 && t * BN + key0 + key < kvl && start + sl < a.max_pos;
+          vs[blk] = (flag & 3) == 3 && t * BN + key0 + key < kvl && start + sl < a.max_pos;
+          // row start + sl of the fp16 table: cos (64) | sin (64); this thread's 8 frequencies
+          const uint16_t* rg = a.cos_sin16 + (size_t)(vs[blk] ? start + sl : 0) * D;
+          const uint4 c4 = __ldg(reinterpret_cast<const uint4*>(rg + 8 * fg));
+          const uint4 s4 = __ldg(reinterpret_cast<const uint4*>(rg + D / 2 + 8 * fg));
+          cvs[blk] = U4{c4.x, c4.y, c4.z, c4.w};
+          svs[blk] = U4{s4.x, s4.y, s4.z, s4.w};
+        }
+        uint32_t wa = 0u, wb = 0u;  // fp16 range watch over the stored keys
+#pragma unroll
+        for (int blk = 0; blk < kHalfBlocks; ++blk) {
+          const U4 cv = cvs[blk], sv = svs[blk];
+          const int key = blk * 16 + sl;
+          const bool v = vs[blk];
           U4* px = reinterpret_cast<U4*>(sk + swz(key, fg));
           U4* py = reinterpret_cast<U4*>(sk + BH * 128 + swz(key, fg));
           U4 x = *px, y = *py;
-          uint64_t c2[4], s2[4];  // cos/sin((start + sl) theta) by angle addition
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            c2[e] = ptx::sub2(ptx::mul2(ac[e], rsc[e]), ptx::mul2(as[e], rss[e]));
-            s2[e] = ptx::fma2(as[e], rsc[e], ptx::mul2(ac[e], rss[e]));
-          }
-          rot_pack(x, y, c2, s2);
+          rot_pack16(x, y, cv, sv);
           if (v) {
             *px = x;
             *py = y;
+            wa = ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(wa, x.x), x.y), x.z), x.w);
+            wb = ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(wb, y.x), y.y), y.z), y.w);
           }
         }
+        if ((wa | wb) != 0u) atomicOr(a.err, kErrRange);
         ptx::fence_proxy_async_smem();
       }
       __syncwarp();
@@ -529,6 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           s2[2] = ptx::f2(sb.x * qs, sb.y * qs); s2[3] = ptx::f2(sb.z * qs, sb.w * qs);
           rot_pack(qc[c], qc[c + D / 16], c2, s2);
         }
+        uint32_t wq = 0u;  // fp16 range watch over the rotated, scaled query
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c)
+          wq = ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(ptx::watch_h2(wq, qc[c].x), qc[c].y), qc[c].z), qc[c].w);
+        if (row_ok && wq != 0u) atomicOr(a.err, kErrRange);
       } else {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {

@@ -296,6 +296,22 @@ __device__ __forceinline__ uint32_t f2_to_h2(uint64_t v) {
   return pack_f16(lo, hi);
 }
 
+// Packed fp16 pairs: a * b and a * b + c, each rounded once to fp16 (RNE).
+__device__ __forceinline__ uint32_t mul_h2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t fma_h2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// Range watch for fp16 operands: start acc at 0 and fold every packed fp16
+// word w in; acc stays +0 while every lane is finite (finite * 0 + 0 = +0) and
+// becomes NaN once a lane is infinite or NaN (an fp16 overflow: inf * 0 = NaN).
+__device__ __forceinline__ uint32_t watch_h2(uint32_t acc, uint32_t w) { return fma_h2(w, 0u, acc); }
+
 // L2 eviction policies (createpolicy)
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

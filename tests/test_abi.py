@@ -111,6 +111,23 @@ def test_prefill_rejects_f32(lib):
                                     0.0, None, 0, None) == 2
 
 
+def test_prefill_needs_the_fp16_table(lib):
+    kv = _kv()
+    pb = mp._Prefill(0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000, 1, 16, 16, 4, 0xA000, None)
+    for rope in (mp._Rope(0x9000, 1024, 128), mp._Rope(0x9000, 1024, 128, 0xB008)):  # missing, misaligned
+        assert lib.minipic_attn_prefill(1, 4, ctypes.byref(kv), ctypes.byref(rope), ctypes.byref(pb),
+                                        0.0, None, 0, None) == 1
+
+
+def test_rope_table_f16_validation(lib):
+    f = lib.minipic_rope_table_f16
+    assert f(None, 10, 64, 1e4, None) == 1
+    assert f(0x1000, 0, 64, 1e4, None) == 1
+    assert f(0x1000, 10, 63, 1e4, None) == 1
+    assert f(0x1000, 10, 64, 0.0, None) == 1
+    assert f(0x1008, 10, 64, 1e4, None) == 1
+
+
 def test_workspace_size_is_pure_host(lib):
     n = lib.minipic_attn_decode_workspace_size(8, 64, 8, 128, 8192, 16)
     assert n >= 0

@@ -1,5 +1,5 @@
-"""Host-side logic of bench.py that needs no GPU: the single-threaded oracle
-timing behind the reported core count, the DRAM-traffic record that is used
+"""Host-side logic of bench.py that needs no GPU: the oracle pool behind the
+reported core count (single-threaded BLAS in each of one worker per core), the DRAM-traffic record that is used
 only while the kernel sources are unchanged, and the algorithmic work counts."""
 
 import json
@@ -16,7 +16,7 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 
-def test_oracle_blas_runs_on_the_reported_core_count():
+def test_oracle_blas_is_single_threaded_per_worker():
     pytest.importorskip("threadpoolctl")
     code = ("import bench, numpy, threadpoolctl, json; "
             "print(json.dumps([p['num_threads'] for p in threadpoolctl.threadpool_info() "
@@ -27,7 +27,7 @@ def test_oracle_blas_runs_on_the_reported_core_count():
                                                        "MKL_NUM_THREADS")}).stdout
     threads = json.loads(out.strip().splitlines()[-1])
     assert threads, "numpy reports no BLAS library"
-    assert all(t == bench.ORACLE_THREADS for t in threads)
+    assert all(t == bench.ORACLE_BLAS_THREADS == 1 for t in threads)
 
 
 def _fake_tree(tmp_path, src_text):
@@ -110,7 +110,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
     assert d["steps"] == 1 and d["warmup"] == 0 and d["value"] > 0 and d["higher_is_better"] is True
     cb = d["cpu_baseline"]
-    assert cb["value"] == d["value"] and cb["kind"] == "oracle" and cb["cores"] == bench.ORACLE_THREADS
+    assert cb["value"] == d["value"] and cb["kind"] == "oracle" and cb["cores"] == (os.cpu_count() or 1)
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 

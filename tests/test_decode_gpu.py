@@ -40,13 +40,29 @@ def run_decode(env, w, prerotated=False, t=None, rope=None):
 @pytest.mark.parametrize("d,base,max_pos", [(64, 10000.0, 129), (128, 500000.0, 131073), (128, 1e6, 32769)])
 def test_rope_table_within_one_ulp(env, d, base, max_pos):
     torch, mp, dev = env
-    T = mp.rope_table(max_pos, d, base, device=dev).cpu().numpy().astype(np.float64)
+    T = mp.rope_table(max_pos, d, base, device=dev).cos_sin.cpu().numpy().astype(np.float64)
     R = oracle.rope_table(max_pos, d, base)
     ulp = np.spacing(np.abs(R).astype(np.float32)).astype(np.float64)
     # the fp64 angle p*theta carries an absolute error of a few ulp(p*theta) <= ~6e-11;
     # next to zero that is many fp32 ulps, elsewhere the bound is one fp32 ulp
     angle_err = 8 * max_pos * 2.0 ** -52
     assert np.all(np.abs(T - R) <= ulp + angle_err)
+
+
+@pytest.mark.parametrize("d,base,max_pos", [(64, 10000.0, 129), (128, 500000.0, 131073), (128, 1e6, 32769)])
+def test_rope_table_f16_rounds_once_to_nearest(env, d, base, max_pos):
+    """The fp16 table is the exact value rounded once to the nearest fp16: within
+    half an fp16 spacing of the oracle's float64 value (spacing 2^-24 below
+    2^-14, where fp16 numbers are subnormal), plus the fp64 angle error; and its
+    fp16 neighbours are not closer."""
+    torch, mp, dev = env
+    T = mp.rope_table(max_pos, d, base, device=dev).cos_sin_f16.cpu().numpy()
+    R = oracle.rope_table(max_pos, d, base)
+    Th = T.astype(np.float64)
+    spacing = np.spacing(np.abs(Th).astype(np.float16)).astype(np.float64)
+    angle_err = 8 * max_pos * 2.0 ** -52
+    assert np.all(np.abs(Th - R) <= 0.5 * spacing + angle_err)
+    assert np.all(np.isfinite(Th)) and np.all(np.abs(Th) <= 1.0)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

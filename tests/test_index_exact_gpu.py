@@ -22,9 +22,12 @@ from index_codes import (ALIGNED, aligned_decode, coded_values, counts, counts_f
 
 pytestmark = pytest.mark.gpu
 
-# distance of n * out from the nearest integer allowed before the rounding is
-# trusted: fp32 outputs carry ~1e-7 relative error, bf16 outputs 2^-9
-FRAC = {"f32": 1e-3, "bf16": 0.3}
+# How far n * out may sit from the exact count c: fp32 outputs carry ~1e-7
+# relative error, bf16 outputs a rounding of at most 2^-9 relative (plus the
+# fp32 sums before it).  Counts are kept below 110 in the bf16 cases, so the
+# bound stays under 1/2 and the nearest integer is the count.
+def _tol(c, dtype):
+    return 1e-3 + 0.0 * c if dtype == "f32" else 2.0 ** -8 * c + 0.05
 
 
 @pytest.fixture(scope="module")
@@ -67,13 +70,16 @@ def _check_row(got, ref, phys, slot, n, g, dtype, what):
     if n == 0:
         assert np.all(got == 0.0), what
         return
-    cg, fg = counts(got, n)
+    cg, _ = counts(got, n)
     cr, fr = counts(ref, n)
     assert fr < 1e-4, f"{what}: oracle counts not integral ({fr})"
-    assert fg <= FRAC[dtype], f"{what}: GPU counts not integral ({fg})"
     exp = counts_from_indices(phys, slot, d)
+    tol = _tol(exp, dtype)
+    assert np.all(tol < 0.5), f"{what}: counts too large to resolve in {dtype}"
     assert np.array_equal(cr, exp), f"{what}: oracle counts differ from its index map"
     assert np.array_equal(cg, exp), f"{what}: gathered set differs: {np.nonzero(cg != exp)[0]}"
+    x = np.asarray(got[:-1], dtype=np.float64) * n
+    assert np.all(np.abs(x - exp) <= tol), f"{what}: counts off by {np.abs(x - exp).max()}"
     assert abs(got[-1] - (g + 1)) <= 1e-5 * (g + 1) + (2.0 ** -8 if dtype == "bf16" else 0.0), f"{what}: kv head"
 
 
@@ -104,7 +110,7 @@ def test_decode_gathers_exactly_in_a_large_batch(env):
     """The same with enough requests that the grid spans several waves and
     splits of different lengths."""
     rng = np.random.default_rng(7)
-    lens = rng.integers(0, 3000, size=96).tolist()
+    lens = rng.integers(0, 1500, size=96).tolist()
     w = zero_query_decode(41, "bf16", 32, 8, 128, lens)
     out, _ = _decode_gpu(env, w)
     ref, _ = oracle.decode(w)

@@ -150,3 +150,47 @@ def test_prefill_repeats_bit_for_bit(env, case):
         out, lse = run_prefill(env, w)
         assert np.array_equal(out, first) and np.array_equal(lse, first_lse, equal_nan=True)
     assert env[1].device_error() == 0
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("where", ["key", "query"])
+def test_fp16_range_overflow_is_flagged(env, d, where):
+    """The QK^T operands are fp16: a rotated key element, or a rotated and
+    scaled query element, beyond +-65504 sets MINIPIC_DEVERR_RANGE (16).  Rows
+    that read the element are undefined; every other row stays finite and
+    matches the oracle."""
+    torch, mp, dev = env
+    w = W.irregular_prefill(77 + d, "bf16", kv_lens=[300, 200, 90], q_lens=[200, 200, 90], Hq=8, Hkv=2, d=d,
+                            max_pos=30000)
+    p = w.prefill
+    G = w.Hq // w.Hkv
+    big = W.to_bf16_bits(np.array([2.0e6], dtype=np.float32))[0]  # > 65504 / (scale log2 e) as well
+    bad = np.zeros((int(p.cu_q_lens[-1]), w.Hq), dtype=bool)  # (query row, head) that read the element
+    if where == "key":
+        j0 = 250  # key 250 of request 0: block 15, slot 10, kv head 1, element 3
+        phys, slot = int(p.block_tables[0, j0 // 16]), j0 % 16
+        w.kv.k_pool[phys, 1, slot, 3] = big
+        for r in range(p.batch):
+            kv, q0, q1 = int(p.kv_lens[r]), int(p.cu_q_lens[r]), int(p.cu_q_lens[r + 1])
+            ph, sl, _ = oracle.key_index_map(p.block_tables[r], p.block_starts[r], kv, 16)
+            hits = np.nonzero((ph == phys) & (sl == slot))[0]
+            for i in range(q1 - q0):
+                if hits.size and hits.min() <= kv - (q1 - q0) + i:
+                    bad[q0 + i, G:2 * G] = True
+    else:
+        row = int(p.cu_q_lens[1]) + 7  # request 1, chunk query 7, head 5
+        p.q[row, 5, 2] = big
+        bad[row, 5] = True
+    mp.device_error(clear=True)
+    out, _ = run_prefill(env, w)
+    assert mp.device_error(clear=True) & 16
+    ref, _ = oracle.prefill(w)
+    ok = ~bad
+    assert ok.sum() > 0.5 * ok.size
+    assert np.all(np.isfinite(out[ok]))
+    compare(out[ok], ref[ok], "bf16", f"rows away from the {where} overflow")
+    # the same inputs without the large element raise no flag
+    w2 = W.irregular_prefill(77 + d, "bf16", kv_lens=[300, 200, 90], q_lens=[200, 200, 90], Hq=8, Hkv=2, d=d,
+                             max_pos=30000)
+    run_prefill(env, w2)
+    assert mp.device_error(clear=True) == 0

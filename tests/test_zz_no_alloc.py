@@ -44,7 +44,7 @@ def _noalloc(env, w, t, rope):
     out = torch.full_like(t["q"], float("nan"))
     lse = torch.full((d.batch, w.Hq), float("nan"), dtype=torch.float32, device=dev)
     kv = mp._KV(t["k_pool"].data_ptr(), t["v_pool"].data_ptr(), *t["k_pool"].shape)
-    rp = mp._Rope(rope.data_ptr(), rope.shape[0], rope.shape[1])
+    rp = mp._Rope(rope.cos_sin.data_ptr(), rope.max_pos, rope.head_dim)
     db = mp._Decode(t["q"].data_ptr(), t["block_tables"].data_ptr(), t["block_starts"].data_ptr(),
                     t["seq_lens"].data_ptr(), t["q_pos"].data_ptr(), d.batch, t["block_tables"].shape[1],
                     out.data_ptr(), lse.data_ptr())
