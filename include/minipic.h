@@ -51,6 +51,8 @@
  *  reports MINIPIC_DEVERR_TIMEOUT, zero it again before reuse).  All calls are asynchronous on the
  *  given stream (cudaStream_t; NULL = legacy default stream) and act on the
  *  device current at the call.  Inputs must stay valid until the work completes.
+ *  The library looks up the device address of its error word once per device
+ *  and keeps it: do not use it across cudaDeviceReset on that device.
  *
  * Errors
  * ------
@@ -229,7 +231,10 @@ minipic_status minipic_attn_decode_prerotated(minipic_dtype dtype, int32_t num_q
  *    device current; make that first call before any stream capture.
  *  - All calls on a device share the array and it keeps the last call's
  *    contents (no part of it needs to start at zero).  Calls whose work
- *    overlaps on the GPU race on it: serialize them. */
+ *    overlaps on the GPU race on it: serialize them.
+ *  - The looked-up address is kept for the life of the process: do not use
+ *    the library across cudaDeviceReset (or any teardown of the device's
+ *    primary context) on that device. */
 #define MINIPIC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 minipic_status minipic_attn_decode_noalloc(minipic_dtype dtype, int32_t num_q_heads,
                                            const minipic_kv_pool* kv, const minipic_rope* rope,

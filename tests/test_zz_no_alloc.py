@@ -6,8 +6,13 @@ synchronize or fail, a plain C host).  It keeps split-KV partial results in a
 fixed device array inside the library.  This test calls it through the C ABI
 twice in a row on different inputs (so the second call runs over the first
 call's leftover scratch contents) and compares each result with
-minipic_attn_decode given a caller workspace.  The file sorts last so that a
-run stopping at the first failure has run every other test before it.
+minipic_attn_decode given a caller workspace.  The calls cover both decode
+paths that use split-KV scratch (the bf16 tensor-core kernel, which merges its
+splits itself, and the fp32 kernel with its separate merge kernel), and a call
+with more split counters than the one before, whose counter region lands on
+the earlier call's partial results (the entry point clears it).  The file
+sorts last so that a run stopping at the first failure has run every other
+test before it.
 """
 
 import ctypes
@@ -62,10 +67,12 @@ def _regular(env, w, t, rope):
     return out, lse
 
 
-def test_noalloc_decode_matches_regular_on_two_calls_in_a_row(env):
+def test_noalloc_decode_matches_regular_on_calls_in_a_row(env):
     torch, mp, fn, dev = env
-    cases = [W.long_decode(40, "bf16", B=2, n_spans=3, span_tokens=4096, pool_spans=4),
-             W.rag_decode(41, "bf16", B=5, n_spans=5, span_tokens=256, pool_spans=12, tail_tokens=99)]
+    cases = [W.long_decode(40, "bf16", B=2, n_spans=3, span_tokens=4096, pool_spans=4),    # 16 counters
+             W.rag_decode(41, "bf16", B=5, n_spans=5, span_tokens=256, pool_spans=12, tail_tokens=99),
+             W.rag_decode(42, "f32", B=12, n_spans=4, span_tokens=256, pool_spans=10, tail_tokens=37),
+             W.rag_decode(43, "f32", B=3, n_spans=6, span_tokens=512, pool_spans=9, tail_tokens=5)]
     for w in cases:
         t = upload_decode(w, torch, dev)
         rope = mp.rope_table(w.max_pos, w.d, w.rope_base, device=dev)
@@ -76,10 +83,14 @@ def test_noalloc_decode_matches_regular_on_two_calls_in_a_row(env):
         torch.cuda.synchronize()
         a, b = o1.float().cpu().numpy(), o2.float().cpu().numpy()
         assert np.all(np.isfinite(a))
+        tol = TOL[w.dtype]
         diff = np.abs(a - b)
-        assert diff.max() <= TOL["bf16"]["max_abs"] and diff.mean() <= TOL["bf16"]["mean_abs"]
-        assert np.abs(l1.cpu().numpy() - l2.cpu().numpy()).max() <= TOL["bf16"]["lse"]
+        assert diff.max() <= tol["max_abs"] and diff.mean() <= tol["mean_abs"]
+        assert np.abs(l1.cpu().numpy() - l2.cpu().numpy()).max() <= tol["lse"]
         assert mp.device_error() == 0
+    # the third call's counters (96 of them: 512 bytes) covered bytes that the
+    # second call (40 counters: 256 bytes) had filled with partial results
+    assert -(-12 * 8 * 4 // 256) * 256 > -(-5 * 8 * 4 // 256) * 256
 
 
 def test_noalloc_rejects_shapes_beyond_the_fixed_scratch(env):
