@@ -24,7 +24,9 @@
 // two thirds of it.  Every stage and barrier lives in both CTAs at the same
 // offsets; CTA 0's barriers gather what its tensor core waits for.
 //
-// Roles in each CTA (15 warps):
+// Roles in each CTA (16 warps; at the top of its branch each warpgroup sets
+// its register budget with setmaxnreg: softmax 176, rotation 96, the rest 64,
+// so that the softmax keeps its 80 scores per thread in registers):
 //   warps 0-7   softmax: warp w covers TMEM lanes 32 (w % 4).. (query rows)
 //               and keys 80 (w / 4) .. +79 of the tile; the two warps of a
 //               lane quarter combine their row maxima through shared memory;
@@ -39,6 +41,7 @@
 //               cluster-scope release per tile, covering what it observed)
 //   warp 14     V producer: this CTA's 64 head dims of every V block by TMA;
 //               both CTAs' copies complete on CTA 0's V barrier
+//   warp 15     idle (completes warpgroup 3 for the register split)
 // (K~ and V have producers of their own, so that K~ tiles run NSK tiles ahead
 // of the products whatever the V stages wait for.)
 // S is double-buffered in TMEM, so QK^T of tile t+1 runs while the softmax
@@ -62,7 +65,10 @@ constexpr int kTileBlocks = 2 * kHalfBlocks;   // blocks of a key tile
 constexpr int BN = 16 * kTileBlocks;           // 160 keys per tile
 constexpr int BH = 16 * kHalfBlocks;           // 80 keys per CTA
 constexpr int kMaskRing = 8;
-constexpr int kThreads = 15 * 32;
+constexpr int kThreads = 16 * 32;
+// registers per thread after the split (the launch gives 128 x 512 = 65536)
+constexpr int kRegSoft = 176, kRegRot = 96, kRegAux = 64;
+static_assert(2 * 128 * kRegSoft + 128 * kRegRot + 128 * kRegAux <= 128 * kThreads, "register split");
 constexpr int kSoftWarps = 8;
 constexpr int kRotBase = 256;  // first thread of the four rotation warps
 constexpr int kTmaWarp = 12, kMmaWarp = 13, kVWarp = 14;
@@ -157,6 +163,15 @@ __device__ __forceinline__ void rot_pack(U4& x, U4& y, const uint64_t (&c2)[4], 
 __device__ __forceinline__ void arrive_leader(uint32_t bar, uint32_t crank) {
   if (crank == 0) ptx::mbar_arrive(bar);
   else ptx::mbar_arrive_peer(bar, 0);
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 template <bool ROPE, int NSK, int NSV>
@@ -262,172 +277,178 @@ __global__ void __launch_bounds__(kThreads, 1)
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
 
-  if (warp == kTmaWarp) {
-    // ======================================================== K~ producer
-    // Step u loads K~ tile u (this CTA's five blocks, once QK(u - NSK) freed
-    // the stage) and publishes the key-valid bits and V block ids of tile u
-    // in ring slot u % 8.  Lanes 0-9 hold the table entries of the tile's
-    // blocks.  The slot is rewritten for tile u + 8 only after QK(u + 4),
-    // which follows PV(u + 2): every reader is past tile u by then.
-    if (n_kt > 0) {
-      const int* bt = a.block_tables + (size_t)r * mb;
-      const int* bs = a.block_starts + (size_t)r * mb;
-      const int kb = lane % kHalfBlocks, hh = lane / kHalfBlocks;   // copy lanes: block, 64-column half
-      const int src = kHalfBlocks * (int)crank + kb;               // lane holding that block's entries
-      const int own = lane - kHalfBlocks * (int)crank;             // 0..4 on this CTA's block lanes
-      const bool mine = own >= 0 && own < kHalfBlocks;
-      int my_ph = -1, my_st = 0;
-      auto fetch = [&](int u) {
-        const int b = kTileBlocks * u + lane;
-        const bool in = lane < kTileBlocks && b < nblk;
-        my_ph = in ? __ldg(bt + b) : -1;
-        my_st = in ? __ldg(bs + b) : 0;
-      };
-      bool ok = true;
-      my_ph = lane < kTileBlocks && lane < nblk ? pre_ph : -1;  // tile 0, loaded before the setup
-      my_st = lane < kTileBlocks && lane < nblk ? pre_st : 0;
-      for (int u = 0; u < n_kt; ++u) {
-        {
-          const int s = u % NSK;
-          bool w = true;
-          if (lane == 0 && u >= NSK) w = ptx::mbar_wait(bar(P_::B_KFREE + s), ((u / NSK) - 1) & 1);
-          if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
+  // each warpgroup sets its register budget at the top of its own branch, so
+  // that the compiler allocates every role's code within that role's budget
+  if (warp >= kTmaWarp) {
+    regs_dec<kRegAux>();
+    if (warp == kTmaWarp) {
+      // ======================================================== K~ producer
+      // Step u loads K~ tile u (this CTA's five blocks, once QK(u - NSK) freed
+      // the stage) and publishes the key-valid bits and V block ids of tile u
+      // in ring slot u % 8.  Lanes 0-9 hold the table entries of the tile's
+      // blocks.  The slot is rewritten for tile u + 8 only after QK(u + 4),
+      // which follows PV(u + 2): every reader is past tile u by then.
+      if (n_kt > 0) {
+        const int* bt = a.block_tables + (size_t)r * mb;
+        const int* bs = a.block_starts + (size_t)r * mb;
+        const int kb = lane % kHalfBlocks, hh = lane / kHalfBlocks;   // copy lanes: block, 64-column half
+        const int src = kHalfBlocks * (int)crank + kb;               // lane holding that block's entries
+        const int own = lane - kHalfBlocks * (int)crank;             // 0..4 on this CTA's block lanes
+        const bool mine = own >= 0 && own < kHalfBlocks;
+        int my_ph = -1, my_st = 0;
+        auto fetch = [&](int u) {
           const int b = kTileBlocks * u + lane;
-          int flag = 0;  // bit 0: usable block id, bit 1: usable start
-          if (lane < kTileBlocks && b < nblk) {
-            if (my_ph >= 0 && my_ph < a.num_blocks) flag |= 1;
-            else if (mine) atomicOr(a.err, kErrBlockId);
-            if (!ROPE || (my_st >= 0 && my_st < a.max_pos)) flag |= 2;
-          }
-          if (lane < kTileBlocks) {
-            // key-valid bits of block b: below kv_len, usable id and start, start + slot in the table
-            uint32_t bits = 0;
-            if ((flag & 3) == 3) {
-              const int nk = min(16, kvl - 16 * b);
-              bits = nk >= 16 ? 0xffffu : (1u << nk) - 1u;
-              if (ROPE) {
-                const int room = a.max_pos - my_st;
-                bits &= room >= 16 ? 0xffffu : (1u << room) - 1u;
-              }
+          const bool in = lane < kTileBlocks && b < nblk;
+          my_ph = in ? __ldg(bt + b) : -1;
+          my_st = in ? __ldg(bs + b) : 0;
+        };
+        bool ok = true;
+        my_ph = lane < kTileBlocks && lane < nblk ? pre_ph : -1;  // tile 0, loaded before the setup
+        my_st = lane < kTileBlocks && lane < nblk ? pre_st : 0;
+        for (int u = 0; u < n_kt; ++u) {
+          {
+            const int s = u % NSK;
+            bool w = true;
+            if (lane == 0 && u >= NSK) w = ptx::mbar_wait(bar(P_::B_KFREE + s), ((u / NSK) - 1) & 1);
+            if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
+            const int b = kTileBlocks * u + lane;
+            int flag = 0;  // bit 0: usable block id, bit 1: usable start
+            if (lane < kTileBlocks && b < nblk) {
+              if (my_ph >= 0 && my_ph < a.num_blocks) flag |= 1;
+              else if (mine) atomicOr(a.err, kErrBlockId);
+              if (!ROPE || (my_st >= 0 && my_st < a.max_pos)) flag |= 2;
             }
-            mask16[(u % kMaskRing) * kTileBlocks + lane] = (uint16_t)bits;
+            if (lane < kTileBlocks) {
+              // key-valid bits of block b: below kv_len, usable id and start, start + slot in the table
+              uint32_t bits = 0;
+              if ((flag & 3) == 3) {
+                const int nk = min(16, kvl - 16 * b);
+                bits = nk >= 16 ? 0xffffu : (1u << nk) - 1u;
+                if (ROPE) {
+                  const int room = a.max_pos - my_st;
+                  bits &= room >= 16 ? 0xffffu : (1u << room) - 1u;
+                }
+              }
+              mask16[(u % kMaskRing) * kTileBlocks + lane] = (uint16_t)bits;
+            }
+            int* m = meta + P_::META * s;
+            if (mine) {
+              m[own] = my_st;
+              m[kHalfBlocks + own] = flag;
+            }
+            if (lane < kTileBlocks) vblk[(u % kMaskRing) * kTileBlocks + lane] = (flag & 1) ? my_ph : -1;
+            const unsigned kv = __ballot_sync(FULL, mine && (flag & 1));
+            const int ph_l = __shfl_sync(FULL, my_ph, src);
+            __syncwarp();
+            if (lane == 0) {
+              ptx::mbar_arrive(bar(P_::B_MASK + u % kMaskRing));
+              ptx::mbar_arrive_expect_tx(bar(P_::B_KFULL + s), __popc(kv) * 2 * 2048);
+            }
+            __syncwarp();
+            if (lane < 2 * kHalfBlocks) {
+              if ((kv >> src) & 1u)
+                ptx::tma_load_2d(sbase + P_::OFF_K + s * P_::KTILE + hh * (BH * 128) + kb * 2048, &kmap, 64 * hh,
+                                 (ph_l * a.Hkv + hk) * 16, bar(P_::B_KFULL + s));
+            }
+            if (u + 1 < n_kt) fetch(u + 1);
           }
-          int* m = meta + P_::META * s;
-          if (mine) {
-            m[own] = my_st;
-            m[kHalfBlocks + own] = flag;
-          }
-          if (lane < kTileBlocks) vblk[(u % kMaskRing) * kTileBlocks + lane] = (flag & 1) ? my_ph : -1;
-          const unsigned kv = __ballot_sync(FULL, mine && (flag & 1));
-          const int ph_l = __shfl_sync(FULL, my_ph, src);
-          __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive(bar(P_::B_MASK + u % kMaskRing));
-            ptx::mbar_arrive_expect_tx(bar(P_::B_KFULL + s), __popc(kv) * 2 * 2048);
-          }
-          __syncwarp();
-          if (lane < 2 * kHalfBlocks) {
-            if ((kv >> src) & 1u)
-              ptx::tma_load_2d(sbase + P_::OFF_K + s * P_::KTILE + hh * (BH * 128) + kb * 2048, &kmap, 64 * hh,
-                               (ph_l * a.Hkv + hk) * 16, bar(P_::B_KFULL + s));
-          }
-          if (u + 1 < n_kt) fetch(u + 1);
         }
+        if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+      }
+      __syncwarp();
+    } else if (warp == kVWarp) {
+      // ======================================================== V producer
+      // V tile t (this CTA's 64 head dims of all ten blocks) once PV(t - NSV)
+      // freed the stage and the K~ producer published the tile's block ids.  The
+      // copies complete on CTA 0's barrier (CTA 1's through the cta_group::2 form),
+      // so the tensor core that reads both halves waits on one barrier.
+      const uint32_t vfull0 = ptx::mapa(bar(P_::B_VFULL), 0);  // CTA 0's barrier, cluster address
+      bool ok = true;
+      for (int t = 0; t < n_kt; ++t) {
+        const int sv = t % NSV;
+        bool w = true;
+        if (lane == 0) {
+          if (t >= NSV) w = ptx::mbar_wait(bar(P_::B_VFREE + sv), ((t / NSV) - 1) & 1);
+          w = w && ptx::mbar_wait(bar(P_::B_MASK + t % kMaskRing), (t / kMaskRing) & 1);
+        }
+        if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
+        const int ph = lane < kTileBlocks ? vblk[(t % kMaskRing) * kTileBlocks + lane] : -1;
+        const unsigned vv = __ballot_sync(FULL, ph >= 0);
+        const uint32_t vbar = vfull0 + 8u * (uint32_t)sv;
+        if (lane == 0) ptx::mbar_arrive_expect_tx_cl(vbar, __popc(vv) * 2048);
+        __syncwarp();
+        if (ph >= 0)
+          ptx::tma_load_2d_pair(sbase + P_::OFF_V + sv * P_::VTILE + lane * 2048, &vmap, 64 * (int)crank,
+                                (ph * a.Hkv + hk) * 16, vbar);
       }
       if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
-    }
-    __syncwarp();
-  } else if (warp == kVWarp) {
-    // ======================================================== V producer
-    // V tile t (this CTA's 64 head dims of all ten blocks) once PV(t - NSV)
-    // freed the stage and the K~ producer published the tile's block ids.  The
-    // copies complete on CTA 0's barrier (CTA 1's through the cta_group::2 form),
-    // so the tensor core that reads both halves waits on one barrier.
-    const uint32_t vfull0 = ptx::mapa(bar(P_::B_VFULL), 0);  // CTA 0's barrier, cluster address
-    bool ok = true;
-    for (int t = 0; t < n_kt; ++t) {
-      const int sv = t % NSV;
-      bool w = true;
-      if (lane == 0) {
-        if (t >= NSV) w = ptx::mbar_wait(bar(P_::B_VFREE + sv), ((t / NSV) - 1) & 1);
-        w = w && ptx::mbar_wait(bar(P_::B_MASK + t % kMaskRing), (t / kMaskRing) & 1);
-      }
-      if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
-      const int ph = lane < kTileBlocks ? vblk[(t % kMaskRing) * kTileBlocks + lane] : -1;
-      const unsigned vv = __ballot_sync(FULL, ph >= 0);
-      const uint32_t vbar = vfull0 + 8u * (uint32_t)sv;
-      if (lane == 0) ptx::mbar_arrive_expect_tx_cl(vbar, __popc(vv) * 2048);
       __syncwarp();
-      if (ph >= 0)
-        ptx::tma_load_2d_pair(sbase + P_::OFF_V + sv * P_::VTILE + lane * 2048, &vmap, 64 * (int)crank,
-                              (ph * a.Hkv + hk) * 16, vbar);
-    }
-    if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
-    __syncwarp();
-  } else if (warp == kMmaWarp && crank != 0) {
-    // ======================================================== relay (CTA 1)
-    // CTA 0 issues the products, which read the keys this CTA's threads rotated
-    // in place.  The relay observes each tile's rotation with an acquire and
-    // forwards it with a release at cluster scope.
-    if (lane == 0) {
-      for (int u = 0; u < n_kt; ++u) {
-        if (!ptx::mbar_wait(bar(P_::B_KROTL + u % NSK), (u / NSK) & 1)) {
-          atomicOr(a.err, kErrTimeout);
-          break;
+    } else if (warp == kMmaWarp && crank != 0) {
+      // ======================================================== relay (CTA 1)
+      // CTA 0 issues the products, which read the keys this CTA's threads rotated
+      // in place.  The relay observes each tile's rotation with an acquire and
+      // forwards it with a release at cluster scope.
+      if (lane == 0) {
+        for (int u = 0; u < n_kt; ++u) {
+          if (!ptx::mbar_wait(bar(P_::B_KROTL + u % NSK), (u / NSK) & 1)) {
+            atomicOr(a.err, kErrTimeout);
+            break;
+          }
+          ptx::mbar_arrive_remote(bar(P_::B_KROT + u % NSK), 0);
         }
-        ptx::mbar_arrive_remote(bar(P_::B_KROT + u % NSK), 0);
       }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ======================================================== MMA issue (CTA 0)
-    if (lane == 0 && n_kt > 0) {
-      const uint32_t id_qk = ROPE ? umma::idesc_f16_f32(256, BN, false, false)
-                                  : umma::idesc_bf16_f32(256, BN, false, false);
-      const uint32_t id_pv = umma::idesc_bf16_f32(256, D, false, true);
-      // S_(t & 1) = Q K_t^T once both CTAs rotated their halves of tile t; the
-      // stage is released to both producers while a later tile refills it
-      auto qk = [&](int t) -> bool {
-        const int s = t % NSK;
-        if (!ptx::mbar_wait(bar(P_::B_KROTL + s), (t / NSK) & 1) ||
-            !ptx::mbar_wait_cl(bar(P_::B_KROT + s), (t / NSK) & 1))
-          return false;
-        umma::fence_after_sync();
-        const uint32_t kb = sbase + P_::OFF_K + s * P_::KTILE;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma2::mma_ts(tmem + kColS + BN * (t & 1), tmem + kColQ + 8 * ks,
-                        umma::smem_desc_sw128(kb + (ks >> 2) * (BH * 128) + (ks & 3) * 32, 16, 1024), id_qk,
-                        ks > 0 ? 1u : 0u);
-        umma2::commit_mc(bar(P_::B_S + (t & 1)), kPair);
-        if (t + NSK < n_kt) umma2::commit_mc(bar(P_::B_KFREE + s), kPair);
-        return true;
-      };
-      bool ok = ptx::mbar_wait(bar(P_::B_QRDY), 0);
-      if (ok) ok = qk(0);
-      if (ok && n_kt > 1) ok = qk(1);
-      for (int t = 0; t < n_kt && ok; ++t) {
-        const int sv = t % NSV;
-        if (!ptx::mbar_wait(bar(P_::B_P + (t & 1)), (t >> 1) & 1) ||
-            !ptx::mbar_wait(bar(P_::B_VFULL + sv), (t / NSV) & 1)) {
-          ok = false;
-          break;
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ======================================================== MMA issue (CTA 0)
+      if (lane == 0 && n_kt > 0) {
+        const uint32_t id_qk = ROPE ? umma::idesc_f16_f32(256, BN, false, false)
+                                    : umma::idesc_bf16_f32(256, BN, false, false);
+        const uint32_t id_pv = umma::idesc_bf16_f32(256, D, false, true);
+        // S_(t & 1) = Q K_t^T once both CTAs rotated their halves of tile t; the
+        // stage is released to both producers while a later tile refills it
+        auto qk = [&](int t) -> bool {
+          const int s = t % NSK;
+          if (!ptx::mbar_wait(bar(P_::B_KROTL + s), (t / NSK) & 1) ||
+              !ptx::mbar_wait_cl(bar(P_::B_KROT + s), (t / NSK) & 1))
+            return false;
+          umma::fence_after_sync();
+          const uint32_t kb = sbase + P_::OFF_K + s * P_::KTILE;
+  #pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma2::mma_ts(tmem + kColS + BN * (t & 1), tmem + kColQ + 8 * ks,
+                          umma::smem_desc_sw128(kb + (ks >> 2) * (BH * 128) + (ks & 3) * 32, 16, 1024), id_qk,
+                          ks > 0 ? 1u : 0u);
+          umma2::commit_mc(bar(P_::B_S + (t & 1)), kPair);
+          if (t + NSK < n_kt) umma2::commit_mc(bar(P_::B_KFREE + s), kPair);
+          return true;
+        };
+        bool ok = ptx::mbar_wait(bar(P_::B_QRDY), 0);
+        if (ok) ok = qk(0);
+        if (ok && n_kt > 1) ok = qk(1);
+        for (int t = 0; t < n_kt && ok; ++t) {
+          const int sv = t % NSV;
+          if (!ptx::mbar_wait(bar(P_::B_P + (t & 1)), (t >> 1) & 1) ||
+              !ptx::mbar_wait(bar(P_::B_VFULL + sv), (t / NSV) & 1)) {
+            ok = false;
+            break;
+          }
+          umma::fence_after_sync();
+          // O += P_t V_t, one 16-key block per MMA; V stage: [block][16 keys][64 dims]
+          const uint32_t vb = sbase + P_::OFF_V + sv * P_::VTILE;
+  #pragma unroll
+          for (int ks = 0; ks < kTileBlocks; ++ks)
+            umma2::mma_ts(tmem + kColO, tmem + kColS + BN * (t & 1) + 8 * ks,
+                          umma::smem_desc_sw128(vb + ks * 2048, 2048, 1024), id_pv, (t > 0 || ks > 0) ? 1u : 0u);
+          umma2::commit_mc(bar(P_::B_PV), kPair);
+          if (t + NSV < n_kt) umma2::commit_mc(bar(P_::B_VFREE + sv), kPair);
+          if (t + 2 < n_kt) ok = qk(t + 2);  // S_(t & 1) is free once PV(t) has read P_t
         }
-        umma::fence_after_sync();
-        // O += P_t V_t, one 16-key block per MMA; V stage: [block][16 keys][64 dims]
-        const uint32_t vb = sbase + P_::OFF_V + sv * P_::VTILE;
-#pragma unroll
-        for (int ks = 0; ks < kTileBlocks; ++ks)
-          umma2::mma_ts(tmem + kColO, tmem + kColS + BN * (t & 1) + 8 * ks,
-                        umma::smem_desc_sw128(vb + ks * 2048, 2048, 1024), id_pv, (t > 0 || ks > 0) ? 1u : 0u);
-        umma2::commit_mc(bar(P_::B_PV), kPair);
-        if (t + NSV < n_kt) umma2::commit_mc(bar(P_::B_VFREE + sv), kPair);
-        if (t + 2 < n_kt) ok = qk(t + 2);  // S_(t & 1) is free once PV(t) has read P_t
+        if (!ok) atomicOr(a.err, kErrTimeout);
       }
-      if (!ok) atomicOr(a.err, kErrTimeout);
+      __syncwarp();
     }
-    __syncwarp();
   } else if (tid >= kRotBase) {
+    regs_dec<kRegRot>();
     // ======================================================== key rotation
     const int rt = tid - kRotBase;  // 0..127
     // ---- key rotation: thread -> (frequency group fg of 8, slot sl): slot sl
@@ -484,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(P_::B_KROTL + s));
     }
-  } else if (warp < kSoftWarps) {
+  } else {
+    regs_inc<kRegSoft>();
     // ======================================================== softmax
     // Warp w: query rows 32 (w % 4) + lane (TMEM lanes), keys 80 h .. 80 h + 79
     // of each tile (h = w / 4).  The two warps of a lane quarter share the
@@ -692,6 +714,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- epilogue: O / l -> global; this warp writes head dims 64 h .. 64 h + 63
     failed = failed || pv_late;
     bool have = n_kt > 0 && !failed;
+    // wait for the last two P V products in order: a parity wait is only
+    // meaningful for the barrier's current phase or the one before it, and
+    // PV(n_kt - 2) may still be running here (PV(n_kt - 3) is known complete)
+    if (have && n_kt > 1 && !__all_sync(FULL, ptx::mbar_wait(bar(P_::B_PV), (n_kt - 2) & 1))) {
+      have = false;
+      failed = true;
+    }
     if (have && !__all_sync(FULL, ptx::mbar_wait(bar(P_::B_PV), (n_kt - 1) & 1))) {
       have = false;
       failed = true;

@@ -146,7 +146,7 @@ def test_mixed_launch_gathers_exactly_the_oracles_keys(env):
     d, Hq, Hkv = 128, 16, 2
     wp = W.irregular_prefill(60, "bf16", kv_lens=[300, 513, 90], q_lens=[300, 77, 90], Hq=Hq, Hkv=Hkv, d=d,
                              max_pos=60000, pool_blocks=d - 17)
-    wd = W.irregular_decode(61, "bf16", seq_lens=[0, 1, 33, 700, 2000], Hq=Hq, Hkv=Hkv, d=d, max_pos=60000,
+    wd = W.irregular_decode(61, "bf16", seq_lens=[0, 1, 33, 700, 1500], Hq=Hq, Hkv=Hkv, d=d, max_pos=60000,
                             pool_blocks=d - 17)
     wp.prefill.q[:] = 0
     wd.decode.q[:] = 0
