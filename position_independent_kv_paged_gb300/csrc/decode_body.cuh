@@ -136,9 +136,12 @@ struct Smem {
 };
 
 // One decode CTA: (split, kv head hk, request r) with NW working warps of NS
-// stages each.  Threads beyond the working warps (a mixed launch shares the CTA
-// shape of the prefill kernel) only take part in the CTA barriers.
-template <int D, int NT, bool ROPE, int NW = kWarps, int NS = kStages>
+// stages each.  With BAR = 0 every thread of the block takes part in the CTA
+// barriers (__syncthreads) and threads beyond the working warps only do that;
+// with BAR > 0 only the first NW warps call this function and their barriers
+// are the named barrier BAR over NW * 32 threads (the other warps of the block
+// may have left).
+template <int D, int NT, bool ROPE, int NW = kWarps, int NS = kStages, int BAR = 0>
 __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p,
                                            const DecodeArgs& a, const int split, const int hk, const int r,
                                            uint8_t* smem_raw) {
@@ -153,6 +156,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g8 = lane >> 2, tig = lane & 3;
+  const int nthr = BAR > 0 ? NW * 32 : (int)blockDim.x;  // threads in the CTA barriers
+  auto cta_sync = [&]() {
+    if constexpr (BAR > 0) ptx::named_sync(BAR, NW * 32);
+    else __syncthreads();
+  };
   const int G = a.G;
   const bool worker = warp < NW;
   const int mb = a.max_blocks;
@@ -175,7 +183,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   {
     const int* bt = a.block_tables + (size_t)r * mb + b_begin;
     const int* bs_ = a.block_starts + (size_t)r * mb + b_begin;
-    for (int i = threadIdx.x; i < span; i += blockDim.x) {
+    for (int i = threadIdx.x; i < span; i += nthr) {
       meta[2 * i] = __ldg(bt + i);
       meta[2 * i + 1] = ROPE ? __ldg(bs_ + i) : 0;
     }
@@ -256,7 +264,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
       for (int k = 0; k < 4; ++k) oacc[mt][nt][k] = 0.f;
   }
 
-  __syncthreads();  // meta visible, barriers initialised
+  cta_sync();  // meta visible, barriers initialised
 
   // lane 0: issue the k-th block of this warp into its stage: K and V tiles by
   // TMA, plus the table row |t - start| the block's query rotation needs
@@ -509,10 +517,10 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
           wo[head * OST + 16 * mt + g8 + 8] = oacc[mt][nt][2 + j];
         }
   }
-  __syncthreads();
+  cta_sync();
 
   const bool direct = (n_valid == 1);
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < G * D; idx += nthr) {
     const int head = idx / D, dim = idx - head * D;
     float M = -CUDART_INF_F;
 #pragma unroll
@@ -546,16 +554,16 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   // the last split of this (request, kv head) to finish merges all of them
   // (log-sum-exp across splits) and resets the counter for the next call
   __shared__ int s_last;
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     __threadfence();
     const int old = atomicAdd(a.counters + (size_t)r * a.Hkv + hk, 1);
     s_last = old == n_valid - 1;
   }
-  __syncthreads();
+  cta_sync();
   if (!s_last) return;
   __threadfence();
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < G * D; idx += nthr) {
     const int head = idx / D, dim = idx - head * D;
     const int hq = hk * G + head;
     const size_t base = ((size_t)r * a.Hq + hq) * a.n_split;

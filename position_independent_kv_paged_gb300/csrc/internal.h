@@ -73,6 +73,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, bool rotate, cudaStream_t s)
 cudaError_t launch_prefill_pair(const PrefillArgs& a, bool rotate, cudaStream_t s);
 // One grid of prefill tiles followed by decode splits (both with rotation).
 cudaError_t launch_mixed(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s);
+// Head dim 128: one grid of CTA-pair prefill clusters and decode clusters.
+cudaError_t launch_mixed_pair(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s);
 
 // Cache append: token i of request r -> key index kv_start[r] + i.
 struct AppendArgs {

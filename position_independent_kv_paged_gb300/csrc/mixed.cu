@@ -59,7 +59,7 @@ cudaError_t launch_t(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s) 
 }  // namespace
 
 cudaError_t launch_mixed(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s) {
-  if (p.D == 128) return d.G <= 8 ? launch_t<128, 1>(p, d, s) : launch_t<128, 2>(p, d, s);
+  if (p.D == 128) return launch_mixed_pair(p, d, s);
   return d.G <= 8 ? launch_t<64, 1>(p, d, s) : launch_t<64, 2>(p, d, s);
 }
 

@@ -49,6 +49,7 @@
 // O is rescaled only when a row maximum grows by more than 2^8.
 #include <math_constants.h>
 
+#include "decode_body.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmap.cuh"
@@ -174,12 +175,12 @@ __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// One CTA of the pair that computes query-tile pair `pair` of request r and kv
+// head hk (both CTAs of a cluster call it with the same item).
 template <bool ROPE, int NSK, int NSV>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const PairLaunch L) {
+__device__ __forceinline__ void pair_cta(const CUtensorMap& kmap, const CUtensorMap& vmap, const PairLaunch& L,
+                                         const int pair, const int hk, const int r, uint8_t* smem_raw) {
   using P_ = PP<NSK, NSV>;
-  extern __shared__ uint8_t smem_raw[];
   const PrefillArgs& a = L.a;
   const uint32_t sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
   uint8_t* sg = smem_raw + (sbase - ptx::smem_addr(smem_raw));
@@ -195,8 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = ptx::cluster_rank();
-  const int pair = L.n_pairs - 1 - (int)(blockIdx.x >> 1);  // heaviest (latest) pairs first
-  const int hk = blockIdx.y, r = blockIdx.z;
   const int G = a.G, TQ = L.tq, mb = a.max_blocks;
   const int q0 = a.cu_q_lens[r];
   const int ql = a.cu_q_lens[r + 1] - q0;
@@ -769,6 +768,87 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::cluster_sync_relaxed();  // neither CTA leaves while the pair's TMEM is being released
 }
 
+template <bool ROPE, int NSK, int NSV>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const PairLaunch L) {
+  extern __shared__ uint8_t smem_raw[];
+  // heaviest (latest) query-tile pairs first
+  pair_cta<ROPE, NSK, NSV>(kmap, vmap, L, L.n_pairs - 1 - (int)(blockIdx.x >> 1), blockIdx.y, blockIdx.z, smem_raw);
+}
+
+// Mixed continuous batch in one launch (the device side of interleaved
+// span-prefill scheduling, MiniPIC summary section 2.2 "Scheduling": span
+// prefills pipelined with ongoing decodes).  Every cluster of the grid is
+// either a prefill cluster (one query-tile pair, the CTA-pair body above) or a
+// decode cluster (each of its two CTAs one decode split, the decode kernel's
+// CTA body run by warps 0-7 with 232 registers each while warps 8-15 give
+// their registers up and leave).  The decode clusters come first in the grid
+// and the prefill clusters (heaviest first) follow, so that the long prefill
+// clusters fill the SMs as the short decode CTAs drain (measured against
+// prefill first and against decode clusters spread evenly through the grid,
+// this order was the fastest).
+constexpr int kMixDecWarps = 8, kMixDecStages = 3, kMixDecBar = 8;
+constexpr int kRegMixDec = 232, kRegMixIdle = 24;
+static_assert(2 * 128 * kRegMixDec + 2 * 128 * kRegMixIdle <= 128 * kThreads, "decode register split");
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    mixed_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      const PairLaunch L, const DecodeArgs Dd, const int n_pre, const int n_dec) {
+  extern __shared__ uint8_t smem_raw[];
+  const long long c = blockIdx.x >> 1;
+  const long long d0 = c < n_dec ? c : n_dec;  // decode clusters before cluster c
+  if (c < n_dec) {
+    if ((threadIdx.x >> 5) >= kMixDecWarps) {
+      regs_dec<kRegMixIdle>();
+      return;
+    }
+    regs_inc<kRegMixDec>();
+    const int u = 2 * (int)d0 + (int)ptx::cluster_rank();  // decode unit: (split, kv head, request)
+    if (u >= Dd.n_split * Dd.Hkv * Dd.batch) return;
+    const int split = u % Dd.n_split, rest = u / Dd.n_split;
+    decode_impl::decode_cta<D, NT, true, kMixDecWarps, kMixDecStages, kMixDecBar>(&kmap, &vmap, Dd, split,
+                                                                                 rest % Dd.Hkv, rest / Dd.Hkv,
+                                                                                 smem_raw);
+  } else {
+    const int i = (int)(c - d0);  // prefill item: (request, kv head) groups, heaviest pairs first
+    const int grp = i / L.n_pairs;
+    pair_cta<true, kNSK, kNSV>(kmap, vmap, L, L.n_pairs - 1 - (i - grp * L.n_pairs), grp % L.a.Hkv, grp / L.a.Hkv,
+                               smem_raw);
+  }
+}
+
+template <int NT>
+cudaError_t launch_mixed_t(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s) {
+  constexpr int sa = PP<kNSK, kNSV>::TOTAL, sb = decode_impl::Smem<D, kMixDecWarps, kMixDecStages>::TOTAL;
+  const int smem = (sa > sb ? sa : sb) + 1024;
+  static bool done[64] = {false};
+  cudaError_t e = set_smem_once(mixed_pair_kernel<NT>, smem, done);
+  if (e != cudaSuccess) return e;
+  CUtensorMap km, vm;
+  const long long rows = (long long)p.num_blocks * p.Hkv * 16;
+  if (!make_pool_map(&km, p.k_pool, rows, D) || !make_pool_map(&vm, p.v_pool, rows, D)) return cudaErrorInvalidValue;
+  PairLaunch L{p, 128 / p.G, 0};
+  L.n_pairs = (p.max_q_len + 2 * L.tq - 1) / (2 * L.tq);
+  const long long n_pre = (long long)L.n_pairs * p.Hkv * p.batch;
+  const long long n_dec = ((long long)d.n_split * d.Hkv * d.batch + 1) / 2;
+  if (n_pre + n_dec > 0x3fffffffLL) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * (n_pre + n_dec)), 1, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mixed_pair_kernel<NT>, km, vm, L, d, (int)n_pre, (int)n_dec);
+}
+
 template <bool ROPE>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   using P_ = PP<kNSK, kNSV>;
@@ -801,6 +881,11 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
 cudaError_t launch_prefill_pair(const PrefillArgs& a, bool rotate, cudaStream_t s) {
   if (a.D != D) return cudaErrorInvalidValue;
   return rotate ? launch_t<true>(a, s) : launch_t<false>(a, s);
+}
+
+cudaError_t launch_mixed_pair(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s) {
+  if (p.D != D || d.D != D) return cudaErrorInvalidValue;
+  return d.G <= 8 ? launch_mixed_t<1>(p, d, s) : launch_mixed_t<2>(p, d, s);
 }
 
 }  // namespace minipic
