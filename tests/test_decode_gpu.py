@@ -1,11 +1,14 @@
 """Decode parity: the CUDA path (through the C ABI) against the CPU oracle."""
 
+import os
+
 import numpy as np
 import pytest
 
 import oracle
 import workloads as W
 from gpu_util import TOL, compare, compare_lse, upload_decode, to_dev, i32
+from oracle_pool import OraclePool
 
 pytestmark = pytest.mark.gpu
 
@@ -189,14 +192,19 @@ def test_device_checks_flag_bad_block_ids_and_positions(env):
 
 # ---------------------------------------------------------------- full sizes (sampled outputs)
 
-@pytest.mark.parametrize("idx,sample", [(1, [0, 31, 63]), (3, [2]), (4, [0, 77, 127])])
-def test_full_size_decode_sampled(env, idx, sample):
+@pytest.mark.parametrize("idx,sample", [(1, list(range(0, 64, 4))), (3, list(range(8))),
+                                        (4, list(range(0, 128, 8)))])
+def test_full_size_decode(env, idx, sample):
+    """The full workloads in the bench's launch configuration: 16 of the 64
+    RAG requests, all 8 long-context requests, 16 of the mixed batch's 128
+    decodes, each against the oracle (run on every host core)."""
     torch, mp, dev = env
     w = W.config(idx)
     if idx == 4:
         w.prefill = None
     out, lse = run_decode(env, w)
-    ref, rl = oracle.decode(w, requests=sample)
+    with OraclePool(w, n_workers=min(len(sample), os.cpu_count() or 1)) as op:
+        ref, rl = op.decode(sample)
     compare(out[sample], ref[sample], "bf16", f"config {idx} sampled")
     compare_lse(lse[sample], rl[sample], "bf16", f"config {idx} sampled")
     assert np.all(np.isfinite(out))

@@ -7,6 +7,7 @@ import pytest
 import oracle
 import workloads as W
 from gpu_util import compare, compare_lse, i32, to_dev
+from oracle_pool import OraclePool
 
 pytestmark = pytest.mark.gpu
 
@@ -85,15 +86,19 @@ def test_mixed_equals_separate_calls(env):
     assert diff.max() <= 4e-3 and diff.mean() <= 2e-4
 
 
-def test_full_size_mixed_sampled(env):
+def test_full_size_mixed(env):
+    """The full mixed batch in one launch: 4 of its 16 span prefills and 16 of
+    its 128 decodes against the oracle (run on every host core)."""
     w = W.config(4)
     po, pl, do, dl, _ = run_mixed(env, w)
-    rp, rpl = oracle.prefill(w, requests=[0, 15])
-    rd, rdl = oracle.decode(w, requests=[0, 77, 127])
+    pre, dec = [0, 5, 10, 15], list(range(3, 128, 8))
+    with OraclePool(w) as op:
+        rp, rpl = op.prefill(pre)
+        rd, rdl = op.decode(dec)
     p = w.prefill
-    rows = np.concatenate([np.arange(p.cu_q_lens[r], p.cu_q_lens[r + 1]) for r in (0, 15)])
+    rows = np.concatenate([np.arange(p.cu_q_lens[r], p.cu_q_lens[r + 1]) for r in pre])
     compare(po[rows], rp[rows], "bf16", "mixed full prefill")
-    compare(do[[0, 77, 127]], rd[[0, 77, 127]], "bf16", "mixed full decode")
-    compare_lse(dl[[0, 77, 127]], rdl[[0, 77, 127]], "bf16", "mixed full decode")
+    compare(do[dec], rd[dec], "bf16", "mixed full decode")
+    compare_lse(dl[dec], rdl[dec], "bf16", "mixed full decode")
     assert np.all(np.isfinite(po)) and np.all(np.isfinite(do))
     assert env[1].device_error() == 0

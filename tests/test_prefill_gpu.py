@@ -1,12 +1,15 @@
 """Chunked-prefill parity: the tcgen05 CUDA path (through the C ABI) against the
 CPU oracle, on RAG-shaped, causal-from-zero and irregular inputs."""
 
+import os
+
 import numpy as np
 import pytest
 
 import oracle
 import workloads as W
 from gpu_util import TOL, compare, compare_lse, upload_prefill
+from oracle_pool import OraclePool
 
 pytestmark = pytest.mark.gpu
 
@@ -82,13 +85,16 @@ def test_prefill_flags_bad_block_ids(env):
     assert np.all(np.isfinite(out))
 
 
-@pytest.mark.parametrize("idx,sample", [(2, [0, 5]), (4, [3, 12])])
-def test_full_size_prefill_sampled(env, idx, sample):
+@pytest.mark.parametrize("idx,sample", [(2, list(range(8))), (4, [0, 3, 7, 12, 15])])
+def test_full_size_prefill(env, idx, sample):
+    """The full RAG prefill (all 8 requests) and 5 of the mixed batch's 16 span
+    prefills, against the oracle run on every host core."""
     w = W.config(idx)
     if idx == 4:
         w.decode = None
     out, lse = run_prefill(env, w)
-    ref, rl = oracle.prefill(w, requests=sample)
+    with OraclePool(w, n_workers=min(len(sample), os.cpu_count() or 1)) as op:
+        ref, rl = op.prefill(sample)
     rows = np.concatenate([np.arange(w.prefill.cu_q_lens[r], w.prefill.cu_q_lens[r + 1]) for r in sample])
     compare(out[rows], ref[rows], "bf16", f"config {idx} sampled")
     compare_lse(lse[rows], rl[rows], "bf16", f"config {idx} sampled")
