@@ -25,6 +25,11 @@ Readings of points the pages leave open (each is listed in the design notes):
   * prefill causality is by key index, bottom-right aligned: query i of a
     q_len chunk sees keys j <= kv_len - q_len + i;
   * an empty key set gives output 0 and log-sum-exp -inf.
+
+``oracle.blockhash`` holds the host-side step that feeds the attention its
+tables: the block-hash chain with span separators (SSEP restarts the chain,
+PDEP ties a block to the whole prompt before it; MiniPIC summary section 2.2)
+and the prefix-cache mapping from hashes to physical blocks.
 """
 
 from .rope import inv_freq, rope_angles, rope_cos_sin, rope_table, rope_rotate
