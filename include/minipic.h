@@ -81,7 +81,8 @@ typedef enum {
   MINIPIC_ERR_UNSUPPORTED = 2,  /* a valid configuration this build has no kernel for */
   MINIPIC_ERR_WORKSPACE = 3,    /* workspace is NULL or smaller than the size query returned */
   MINIPIC_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
-  MINIPIC_ERR_DEVICE_CHECK = 5  /* a kernel recorded out-of-range device data (see below) */
+  MINIPIC_ERR_DEVICE_CHECK = 5, /* a kernel recorded out-of-range device data (see below) */
+  MINIPIC_ERR_CAPACITY = 6      /* prefix cache: no free or released block left (or host memory ran out) */
 } minipic_status;
 
 typedef enum { MINIPIC_F32 = 0, MINIPIC_BF16 = 1 } minipic_dtype;
@@ -332,6 +333,57 @@ minipic_status minipic_kv_swap_out(minipic_dtype dtype, const minipic_kv_pool* k
                                    int32_t n, void* host_k, void* host_v, minipic_stream_t stream);
 minipic_status minipic_kv_swap_in(minipic_dtype dtype, const minipic_kv_pool_mut* kv, const int32_t* block_ids,
                                   int32_t n, const void* host_k, const void* host_v, minipic_stream_t stream);
+
+/* ------------------------------------------------------------------ span reuse (host)
+ * The step that feeds the attention its tables (MiniPIC summary, section 2.2):
+ * KV blocks are cached by a hash chain over their tokens, and two special
+ * tokens at the start of a block change the chain.  For full block i of a
+ * prompt (tokens x_i):
+ *   default  h_i = H(h_{i-1}, x_i), with h_{-1} = h_0
+ *   SSEP     h_i = H(h_0, x_i)        the chain restarts: the span is cached
+ *                                     whatever precedes it
+ *   PDEP     h_i = H(h_0, x_{<=i})    the block depends on the whole prompt
+ *                                     before it, across restarts
+ * H(p, t) is 64-bit FNV-1a over p (8 bytes, little endian) and then the tokens
+ * (4 bytes each, little endian).  Users pad spans to block boundaries so that
+ * the special tokens open blocks.  Only full blocks are hashed; a trailing
+ * partial block stays private to its request.  Host memory and host code
+ * only; no GPU is involved. */
+
+/* Hashes of the n_tokens / block_size full blocks of one prompt into hashes
+ * (host, max_hashes capacity); *n_hashes receives their count.  Errors:
+ * INVALID for null pointers, a non-positive block size or too small a
+ * capacity. */
+minipic_status minipic_block_hashes(const int32_t* tokens, int32_t n_tokens, int32_t block_size, int32_t ssep_token,
+                                    int32_t pdep_token, uint64_t h0, uint64_t* hashes, int32_t max_hashes,
+                                    int32_t* n_hashes);
+
+/* A prefix cache over a pool of num_blocks physical blocks: maps a block hash
+ * to the physical block that holds (or will hold) its unrotated keys and
+ * values.  Not thread-safe; the caller serializes calls on one cache. */
+typedef struct minipic_prefix_cache minipic_prefix_cache;
+minipic_status minipic_prefix_cache_create(int32_t num_blocks, minipic_prefix_cache** cache);
+void minipic_prefix_cache_destroy(minipic_prefix_cache* cache);
+
+/* Blocks of one request with n_blocks blocks, the first n_hashed of them full
+ * and hashed (minipic_block_hashes), the rest private: block_table[b] receives
+ * the physical block, block_starts[b] = b * block_size its logical start in
+ * this request, and is_new[b] = 1 when the block's keys and values still have
+ * to be computed and appended (a miss), 0 when the cache already holds them
+ * (one physical block may appear in many requests at different starts, which
+ * the position-free attention reads correctly).  Each listed block gains one
+ * reference.  A miss takes a never-used block, else evicts the unreferenced
+ * cached block released longest ago; when neither exists the call returns
+ * CAPACITY and leaves the cache as it was.  Host arrays of n_blocks entries. */
+minipic_status minipic_prefix_cache_assign(minipic_prefix_cache* cache, const uint64_t* hashes, int32_t n_hashed,
+                                           int32_t n_blocks, int32_t block_size, int32_t* block_table,
+                                           int32_t* block_starts, uint8_t* is_new);
+
+/* Drop one reference per listed block id (a block listed k times loses k).
+ * An unreferenced cached block stays findable until a miss evicts it; a
+ * private one just becomes free.  INVALID (and no change) when an id is out
+ * of range or has fewer references than listed. */
+minipic_status minipic_prefix_cache_release(minipic_prefix_cache* cache, const int32_t* block_ids, int32_t n);
 
 /* Read the device error word (MINIPIC_DEVERR_* bits, 0 if none) of the current
  * device after the work queued on `stream` has finished (this call

@@ -39,6 +39,8 @@ __all__ = [
     "kv_swap_out",
     "kv_swap_in",
     "device_error",
+    "block_hashes",
+    "PrefixCache",
     "STATUS",
 ]
 
@@ -46,7 +48,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libminipic.so")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
-          3: "workspace missing or too small", 4: "CUDA error", 5: "device data out of range"}
+          3: "workspace missing or too small", 4: "CUDA error", 5: "device data out of range",
+          6: "prefix cache full"}
 F32, BF16 = 0, 1
 
 
@@ -142,6 +145,17 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
             fn.argtypes = [ctypes.c_int, ctypes.POINTER(_KV), c_vp, c_i32, c_vp, c_vp, c_vp]
         L.minipic_device_error.restype = ctypes.c_int
         L.minipic_device_error.argtypes = [ctypes.POINTER(c_i32), c_i32, c_vp]
+        L.minipic_block_hashes.restype = ctypes.c_int
+        L.minipic_block_hashes.argtypes = [c_vp, c_i32, c_i32, c_i32, c_i32, ctypes.c_uint64, c_vp, c_i32,
+                                           ctypes.POINTER(c_i32)]
+        L.minipic_prefix_cache_create.restype = ctypes.c_int
+        L.minipic_prefix_cache_create.argtypes = [c_i32, ctypes.POINTER(c_vp)]
+        L.minipic_prefix_cache_destroy.restype = None
+        L.minipic_prefix_cache_destroy.argtypes = [c_vp]
+        L.minipic_prefix_cache_assign.restype = ctypes.c_int
+        L.minipic_prefix_cache_assign.argtypes = [c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]
+        L.minipic_prefix_cache_release.restype = ctypes.c_int
+        L.minipic_prefix_cache_release.argtypes = [c_vp, c_vp, c_i32]
         _lib = L
         return L
 
@@ -491,3 +505,62 @@ def kv_swap_in(host_k, host_v, block_ids, k_pool, v_pool, stream=None):
             raise ValueError(f"{name} must be a contiguous {tuple(shape)} tensor of the pool's dtype")
     _check(L.minipic_kv_swap_in(_dtype_code(k_pool), ctypes.byref(kv), block_ids.data_ptr(), n,
                                 host_k.data_ptr(), host_v.data_ptr(), _stream(stream)), "minipic_kv_swap_in")
+
+
+# ---------------------------------------------------------------- span reuse (host)
+
+def block_hashes(tokens, block_size: int, ssep_token: int, pdep_token: int, h0: int = 0):
+    """uint64 hashes of the full blocks of one prompt (SSEP restarts the chain,
+    PDEP ties a block to the whole prompt before it); see the header."""
+    import numpy as np
+    L = load()
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    n_full = t.size // int(block_size) if block_size > 0 else 0
+    out = np.zeros(max(n_full, 1), dtype=np.uint64)
+    n = ctypes.c_int32(0)
+    _check(L.minipic_block_hashes(t.ctypes.data if t.size else None, int(t.size), int(block_size), int(ssep_token),
+                                  int(pdep_token), ctypes.c_uint64(int(h0) & ((1 << 64) - 1)),
+                                  out.ctypes.data, int(out.size), ctypes.byref(n)), "minipic_block_hashes")
+    return out[:n.value]
+
+
+class PrefixCache:
+    """Hash -> physical block map over a pool of num_blocks blocks (host)."""
+
+    def __init__(self, num_blocks: int):
+        self._L = load()
+        self._h = ctypes.c_void_p(None)
+        _check(self._L.minipic_prefix_cache_create(int(num_blocks), ctypes.byref(self._h)),
+               "minipic_prefix_cache_create")
+
+    def assign(self, hashes, n_blocks: int, block_size: int):
+        """(block_table, block_starts, is_new) of one request: int32, int32,
+        uint8 arrays of n_blocks entries.  Raises MiniPICError (status 6)
+        when the pool is full; the cache is then unchanged."""
+        import numpy as np
+        h = np.ascontiguousarray(hashes, dtype=np.uint64)
+        n = int(n_blocks)
+        tab = np.zeros(max(n, 1), dtype=np.int32)
+        st = np.zeros(max(n, 1), dtype=np.int32)
+        new = np.zeros(max(n, 1), dtype=np.uint8)
+        _check(self._L.minipic_prefix_cache_assign(self._h, h.ctypes.data if h.size else None, int(h.size), n,
+                                                    int(block_size), tab.ctypes.data, st.ctypes.data,
+                                                    new.ctypes.data), "minipic_prefix_cache_assign")
+        return tab[:n], st[:n], new[:n]
+
+    def release(self, block_ids):
+        import numpy as np
+        b = np.ascontiguousarray(block_ids, dtype=np.int32)
+        _check(self._L.minipic_prefix_cache_release(self._h, b.ctypes.data if b.size else None, int(b.size)),
+               "minipic_prefix_cache_release")
+
+    def close(self):
+        if self._h:
+            self._L.minipic_prefix_cache_destroy(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -297,6 +297,7 @@ const char* minipic_status_string(minipic_status status) {
     case MINIPIC_ERR_WORKSPACE: return "workspace missing or too small";
     case MINIPIC_ERR_CUDA: return "CUDA error";
     case MINIPIC_ERR_DEVICE_CHECK: return "device data out of range";
+    case MINIPIC_ERR_CAPACITY: return "prefix cache full";
   }
   return "unknown status";
 }

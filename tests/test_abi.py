@@ -39,7 +39,8 @@ def test_binding_covers_the_entry_points():
     status strings live in STATUS)."""
     for n in mp.__all__:
         assert hasattr(mp, n), n
-    c_only = {"minipic_attn_decode_noalloc", "minipic_status_string"}
+    c_only = {"minipic_attn_decode_noalloc", "minipic_status_string", "minipic_prefix_cache_create",
+              "minipic_prefix_cache_destroy", "minipic_prefix_cache_assign", "minipic_prefix_cache_release"}
     renamed = {"minipic_attn_decode_workspace_size": "decode_workspace_size",
                "minipic_attn_prefill_workspace_size": "prefill_workspace_size"}
     for n in declared_functions():
