@@ -142,6 +142,7 @@ minipic_status build_decode(minipic_dtype dtype, int32_t num_q_heads, const mini
   a.max_blocks = b->max_blocks_per_seq;
   a.split_blocks = plan.split_blocks;
   a.n_split = plan.n_split;
+  a.ctas_per_sm = plan.ctas_per_sm;
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)kv->head_dim);
   a.err = err;
   *out_args = a;
@@ -245,7 +246,7 @@ DecodeWs decode_ws_layout(int batch, int Hq, int Hkv, int D, int n_split) {
 DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs, bool bf16, int num_sms) {
   (void)D;
   (void)bs;
-  DecodePlan p{max_blocks, 1, bf16};
+  DecodePlan p{max_blocks, 1, bf16, 0};
   const long long pairs = (long long)batch * Hkv;
   if (!bf16) {
     // SIMT path: aim for ~4 CTAs per SM, splits of at least 8 blocks
@@ -260,9 +261,13 @@ DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs,
     p.n_split = (max_blocks + p.split_blocks - 1) / p.split_blocks;
     return p;
   }
-  // tensor-core path: CTAs of 4 warps, 2 resident per SM (1 for groups > 8);
-  // ~12 waves of CTAs, each split at least 32 blocks (8 per warp)
-  const long long resident = (long long)num_sms * (G <= 8 ? 2 : 1);
+  // tensor-core path: CTAs of 4 warps; with many (request, kv head) pairs, 3
+  // resident per SM with 2 stages per warp (more warps to hide the per-block
+  // latency when blocks come from L2), else 2 per SM with 3 stages (deeper
+  // per-warp prefetch for HBM-bound long contexts); 1 for groups > 8.  ~12
+  // waves of CTAs, each split at least 32 blocks (8 per warp)
+  p.ctas_per_sm = G > 8 ? 1 : (pairs >= 2LL * num_sms ? 3 : 2);
+  const long long resident = (long long)num_sms * p.ctas_per_sm;
   const long long total = pairs * max_blocks;
   long long est = (total + resident * 12 - 1) / (resident * 12);
   if (est < 32) est = 32;

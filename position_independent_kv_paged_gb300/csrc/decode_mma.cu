@@ -7,32 +7,35 @@ namespace {
 
 using namespace decode_impl;
 
-template <int D, int NT, bool ROPE>
-__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 2 : 1)
+// CPS resident CTAs per SM: 3 with 2 stages per warp, else 3 stages.
+template <int D, int NT, bool ROPE, int CPS>
+__global__ void __launch_bounds__(kWarps * 32, CPS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  decode_cta<D, NT, ROPE>(&kmap, &vmap, a, blockIdx.x, blockIdx.y, blockIdx.z, smem_raw);
+  decode_cta<D, NT, ROPE, kWarps, CPS == 3 ? 2 : kStages>(&kmap, &vmap, a, blockIdx.x, blockIdx.y, blockIdx.z,
+                                                          smem_raw);
 }
 
-template <int D, int NT, bool ROPE>
+template <int D, int NT, bool ROPE, int CPS>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
-  const int smem = Smem<D>::TOTAL + 1024;
+  const int smem = Smem<D, kWarps, CPS == 3 ? 2 : kStages>::TOTAL + 1024;
   static bool done[64] = {false};
-  cudaError_t e = set_smem_once(decode_mma_kernel<D, NT, ROPE>, smem, done);
+  cudaError_t e = set_smem_once(decode_mma_kernel<D, NT, ROPE, CPS>, smem, done);
   if (e != cudaSuccess) return e;
   CUtensorMap km, vm;
   const long long rows = (long long)a.num_blocks * a.Hkv * 16;
   if (!make_pool_map(&km, a.k_pool, rows, D) || !make_pool_map(&vm, a.v_pool, rows, D))
     return cudaErrorInvalidValue;
   dim3 grid(a.n_split, a.Hkv, a.batch);
-  decode_mma_kernel<D, NT, ROPE><<<grid, kWarps * 32, smem, s>>>(km, vm, a);
+  decode_mma_kernel<D, NT, ROPE, CPS><<<grid, kWarps * 32, smem, s>>>(km, vm, a);
   return cudaGetLastError();
 }
 
 template <int D, bool ROPE>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
-  return a.G <= 8 ? launch_t<D, 1, ROPE>(a, s) : launch_t<D, 2, ROPE>(a, s);
+  if (a.G > 8) return launch_t<D, 2, ROPE, 1>(a, s);
+  return a.ctas_per_sm == 3 ? launch_t<D, 1, ROPE, 3>(a, s) : launch_t<D, 1, ROPE, 2>(a, s);
 }
 
 }  // namespace

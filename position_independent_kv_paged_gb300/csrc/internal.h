@@ -25,6 +25,7 @@ struct DecodeArgs {
   int batch, Hq, Hkv, G, D, BS, num_blocks, max_blocks;
   int split_blocks;          // blocks per split
   int n_split;               // splits per (request, kv head)
+  int ctas_per_sm;           // tensor-core decode: 3 (2 stages per warp) or 2 (3 stages) CTAs per SM
   float scale;               // softmax scale (1/sqrt(D) by default)
   int* err;                  // device error word
 };
@@ -61,6 +62,7 @@ struct DecodePlan {
   int split_blocks;
   int n_split;
   bool use_mma;
+  int ctas_per_sm;  // tensor-core path: resident CTAs per SM (3 or 2; 1 for more than 8 heads per group)
 };
 DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs, bool bf16, int num_sms);
 
