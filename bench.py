@@ -130,6 +130,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="minipic", choices=["minipic", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the rope-off, e2e and CPU legs")
+    ap.add_argument("--only", choices=sorted(ONLY_LEGS),
+                    help="run one leg's kernel call warmup + steps times, untimed (for profilers), and exit")
     return ap.parse_args()
 
 
@@ -448,6 +450,61 @@ def timed(torch, stream, flush, fn, steps):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+# Legs --only can run alone: workload, case kind, call.
+ONLY_LEGS = {
+    "decode": ("rag_decode", "decode", "step"),
+    "decode_rope_off": ("rag_decode", "decode", "step_norope"),
+    "private": ("rag_decode_private", "decode", "step"),
+    "private_rope_off": ("rag_decode_private", "decode", "step_norope"),
+    "long": ("long_decode", "decode", "step"),
+    "long_rope_off": ("long_decode", "decode", "step_norope"),
+    "prefill": ("rag_prefill", "prefill", "step"),
+    "prefill_rope_off": ("rag_prefill", "prefill", "step_norope"),
+    "mixed": ("mixed_batch", "mixed", None),
+    "mixed_prefill": ("mixed_batch", "prefill", "step"),
+    "mixed_decode": ("mixed_batch", "decode", "step"),
+}
+
+
+def run_only(args):
+    """One leg's kernel call, warmup + steps times with no timing: the command
+    the profiles are captured from (a profiler then sees only that kernel)."""
+    import torch
+
+    import position_independent_kv_paged_gb300 as mp
+    import workloads as W
+    from position_independent_kv_paged_gb300 import _build
+
+    wname, kind, call = ONLY_LEGS[args.only]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    mp.load()
+    w = {"rag_decode": lambda: W.rag_decode(seed=0), "rag_decode_private": lambda: W.rag_decode(seed=0, share=False),
+         "long_decode": lambda: W.long_decode(seed=0), "rag_prefill": lambda: W.rag_prefill(seed=0),
+         "mixed_batch": lambda: W.mixed_batch(seed=0)}[wname]()
+    if kind == "mixed":
+        cp, cd = PrefillCase(w, dev, torch, mp), DecodeCase(w, dev, torch, mp)
+        cd.kpool, cd.vpool = cp.kpool, cp.vpool
+        pre = dict(q=cp.q, cu_q_lens=cp.cu, q_pos=cp.qp, block_tables=cp.bt, block_starts=cp.st,
+                   kv_lens=cp.kvl, max_q_len=cp.max_q, out=cp.out, lse=cp.lse)
+        dec = dict(q=cd.q, block_tables=cd.bt, block_starts=cd.st, seq_lens=cd.sl, q_pos=cd.qp,
+                   out=cd.out, lse=cd.lse)
+
+        def fn():
+            mp.attn_mixed(pre, dec, cp.kpool, cp.vpool, cp.rope, workspace=cd.ws)
+    else:
+        case = (DecodeCase if kind == "decode" else PrefillCase)(w, dev, torch, mp)
+        fn = getattr(case, call)
+    n = args.warmup + args.steps
+    for _ in range(n):
+        fn()
+    torch.cuda.synchronize()
+    err = mp.device_error()
+    print(json.dumps({"only": args.only, "workload": w.name, "calls": n, "device_error": err}), flush=True)
+    return 0 if err == 0 else 1
+
+
 def run_minipic(args):
     import numpy as np
     import torch
@@ -685,6 +742,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.only:
+        return run_only(args)
     return run_minipic(args)
 
 

@@ -32,7 +32,9 @@
  *    float [max_pos][head_dim], cos(p theta_i) in columns [0, d/2) and
  *    sin(p theta_i) in columns [d/2, d), plus (for the prefill and mixed calls)
  *    the same values rounded to fp16 in a second array of that layout, written
- *    by minipic_rope_table_f16.  Every position used must be < max_pos.
+ *    by minipic_rope_table_f16, and (for the bf16 decode and the mixed call)
+ *    rows of cos | sin | -sin rounded to bf16, written by
+ *    minipic_rope_table_bf16.  Every position used must be < max_pos.
  *  - scale <= 0 selects 1/sqrt(head_dim).
  *  - Outputs: out has the layout of q and the call's dtype; lse (optional, may
  *    be NULL) is float, natural-log log-sum-exp of the scaled scores per
@@ -115,6 +117,11 @@ typedef struct {
                                     minipic_rope_table_f16 with the same max_pos, head_dim
                                     and base; read by the prefill and mixed calls (NULL
                                     there returns INVALID), ignored by decode (may be NULL) */
+  const uint16_t* cos_sin_bf16;  /* [max_pos][2][3 head_dim / 2] bf16 bit patterns, written by
+                                    minipic_rope_table_bf16 with the same max_pos, head_dim
+                                    and base; read by the bf16 decode and the mixed call's
+                                    decode part (NULL there returns INVALID), ignored by the
+                                    fp32 decode and by prefill (may be NULL) */
 } minipic_rope;
 
 /* One decode token per request (MiniPIC section 2.1 score equation with the
@@ -174,6 +181,19 @@ minipic_status minipic_rope_table(float* cos_sin, int32_t max_pos, int32_t head_
  * Errors as for minipic_rope_table. */
 minipic_status minipic_rope_table_f16(uint16_t* cos_sin_f16, int32_t max_pos, int32_t head_dim,
                                       double rope_base, minipic_stream_t stream);
+
+/* The table in the form the bf16 decode's packed-bf16 rotation reads (MiniPIC
+ * section 2.1, the cosine/sine table), over signed angles: for position p and
+ * sign sg (0: +p, 1: -p), row [p][sg] holds 3 head_dim / 2 values, cos, sin and
+ * -sin of the angle (-1)^sg p theta_i at [i], [d/2 + i] and [d + i], i < d/2.
+ * Each is the fp32 table's value (fp64 angle, CUDA's double sincos, rounded to
+ * float) rounded to the nearest bf16 (bit patterns).  A rotation by a signed
+ * angle reads one row: no conversion and no sign logic in the kernel.
+ * cos_sin_bf16: device, at least max_pos * 3 * head_dim uint16 values, 16-byte
+ * aligned, caller-owned; head_dim a multiple of 16.  Errors as for
+ * minipic_rope_table. */
+minipic_status minipic_rope_table_bf16(uint16_t* cos_sin_bf16, int32_t max_pos, int32_t head_dim,
+                                       double rope_base, minipic_stream_t stream);
 
 /* Workspace bytes minipic_attn_decode needs for this shape on the current
  * device (split-KV partial results).  0 means no workspace is needed.  The

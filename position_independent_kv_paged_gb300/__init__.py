@@ -28,6 +28,7 @@ __all__ = [
     "RopeTable",
     "rope_table",
     "rope_table_f16",
+    "rope_table_bf16",
     "decode_workspace_size",
     "attn_decode",
     "attn_decode_prerotated",
@@ -74,7 +75,7 @@ class _Append(ctypes.Structure):
 
 class _Rope(ctypes.Structure):
     _fields_ = [("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("cos_sin_f16", ctypes.c_void_p)]
+                ("cos_sin_f16", ctypes.c_void_p), ("cos_sin_bf16", ctypes.c_void_p)]
 
 
 class _Decode(ctypes.Structure):
@@ -119,6 +120,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         L.minipic_rope_table.argtypes = [c_vp, c_i32, c_i32, c_d, c_vp]
         L.minipic_rope_table_f16.restype = ctypes.c_int
         L.minipic_rope_table_f16.argtypes = [c_vp, c_i32, c_i32, c_d, c_vp]
+        L.minipic_rope_table_bf16.restype = ctypes.c_int
+        L.minipic_rope_table_bf16.argtypes = [c_vp, c_i32, c_i32, c_d, c_vp]
         L.minipic_attn_decode_workspace_size.restype = c_sz
         L.minipic_attn_decode_workspace_size.argtypes = [c_i32] * 6
         L.minipic_attn_decode.restype = ctypes.c_int
@@ -217,14 +220,17 @@ def _kv(k_pool, v_pool) -> _KV:
 # ---------------------------------------------------------------- API
 
 class RopeTable:
-    """The rotary cos/sin table in the two forms the kernels read: ``cos_sin``
-    (float32 [max_pos, head_dim]: decode, and the prefill's query rotation) and
-    ``cos_sin_f16`` (the same values rounded to float16: the prefill's key
-    rotation).  Built by ``rope_table``."""
+    """The rotary cos/sin table in the three forms the kernels read:
+    ``cos_sin`` (float32 [max_pos, head_dim]: the fp32 decode and the prefill's
+    query rotation), ``cos_sin_f16`` (the same values rounded to float16: the
+    prefill's key rotation) and ``cos_sin_bf16`` (bfloat16 [max_pos, 2,
+    3 head_dim / 2]: cos | sin | -sin of +p theta and of -p theta, the bf16
+    decode's rotation).  Built by ``rope_table``."""
 
-    def __init__(self, cos_sin, cos_sin_f16=None):
+    def __init__(self, cos_sin, cos_sin_f16=None, cos_sin_bf16=None):
         self.cos_sin = cos_sin
         self.cos_sin_f16 = cos_sin_f16
+        self.cos_sin_bf16 = cos_sin_bf16
 
     @property
     def max_pos(self) -> int:
@@ -248,20 +254,40 @@ def rope_table_f16(max_pos: int, head_dim: int, base: float, device=None, stream
     return out
 
 
+def rope_table_bf16(max_pos: int, head_dim: int, base: float, device=None, stream=None, out=None):
+    """Build the bfloat16 rows [max_pos, 2, 3 head_dim / 2] on the GPU: [p, 0] is
+    cos | sin | -sin of +p theta_i, [p, 1] the same of -p theta_i."""
+    torch = _torch()
+    L = load()
+    if out is None:
+        out = torch.empty((max_pos, 2, 3 * head_dim // 2), dtype=torch.bfloat16,
+                          device=device if device is not None else "cuda")
+    _need(out, "out", dtype=torch.bfloat16, ndim=3)
+    if tuple(out.shape) != (max_pos, 2, 3 * head_dim // 2):
+        raise ValueError("out must be [max_pos, 2, 3 * head_dim / 2]")
+    _check(L.minipic_rope_table_bf16(out.data_ptr(), int(max_pos), int(head_dim), float(base), _stream(stream)),
+           "minipic_rope_table_bf16")
+    return out
+
+
 def rope_table(max_pos: int, head_dim: int, base: float, device=None, stream=None) -> RopeTable:
-    """Build the cos/sin table (float32 and float16 forms) on the GPU."""
+    """Build the cos/sin table (float32, float16 and bfloat16 forms) on the GPU."""
     torch = _torch()
     L = load()
     f32 = torch.empty((max_pos, head_dim), dtype=torch.float32, device=device if device is not None else "cuda")
     _check(L.minipic_rope_table(f32.data_ptr(), int(max_pos), int(head_dim), float(base), _stream(stream)),
            "minipic_rope_table")
-    return RopeTable(f32, rope_table_f16(max_pos, head_dim, base, device=f32.device, stream=stream))
+    return RopeTable(f32, rope_table_f16(max_pos, head_dim, base, device=f32.device, stream=stream),
+                     rope_table_bf16(max_pos, head_dim, base, device=f32.device, stream=stream))
 
 
-def _rope_struct(rope, need_f16: bool) -> _Rope:
-    """ABI view of a RopeTable (or, for decode, of a bare float32 table)."""
+def _rope_struct(rope, need_f16: bool, need_bf16: bool = False) -> _Rope:
+    """ABI view of a RopeTable (or, for the fp32 decode, of a bare float32 table)."""
     torch = _torch()
-    f32, f16 = (rope.cos_sin, rope.cos_sin_f16) if isinstance(rope, RopeTable) else (rope, None)
+    if isinstance(rope, RopeTable):
+        f32, f16, b16 = rope.cos_sin, rope.cos_sin_f16, rope.cos_sin_bf16
+    else:
+        f32, f16, b16 = rope, None, None
     _need(f32, "rope", dtype=torch.float32, ndim=2)
     if f16 is not None:
         _need(f16, "rope f16", dtype=torch.float16, ndim=2)
@@ -269,7 +295,14 @@ def _rope_struct(rope, need_f16: bool) -> _Rope:
             raise ValueError("the float16 and float32 tables differ in shape")
     elif need_f16:
         raise TypeError("prefill needs the RopeTable built by rope_table() (it carries the float16 table)")
-    return _Rope(f32.data_ptr(), f32.shape[0], f32.shape[1], None if f16 is None else f16.data_ptr())
+    if b16 is not None:
+        _need(b16, "rope bf16", dtype=torch.bfloat16, ndim=3)
+        if tuple(b16.shape) != (f32.shape[0], 2, 3 * f32.shape[1] // 2):
+            raise ValueError("the bfloat16 table must be [max_pos, 2, 3 * head_dim / 2]")
+    elif need_bf16:
+        raise TypeError("the bf16 decode needs the RopeTable built by rope_table() (it carries the bfloat16 table)")
+    return _Rope(f32.data_ptr(), f32.shape[0], f32.shape[1], None if f16 is None else f16.data_ptr(),
+                 None if b16 is None else b16.data_ptr())
 
 
 def decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
@@ -308,7 +341,7 @@ def _decode(q, k_pool, v_pool, block_tables, block_starts, seq_lens, q_pos, rope
                                               float(scale), ws_ptr, ws_n, _stream(stream))
         _check(st, "minipic_attn_decode_prerotated")
     else:
-        rp = _rope_struct(rope, False)
+        rp = _rope_struct(rope, False, need_bf16=q.dtype == torch.bfloat16)
         st = L.minipic_attn_decode(_dtype_code(q), Hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(db),
                                    float(scale), ws_ptr, ws_n, _stream(stream))
         _check(st, "minipic_attn_decode")
@@ -399,7 +432,7 @@ def attn_mixed(prefill: dict, decode: dict, k_pool, v_pool, rope, scale: float =
     torch = _torch()
     L = load()
     kv = _kv(k_pool, v_pool)
-    rp = _rope_struct(rope, True)
+    rp = _rope_struct(rope, True, need_bf16=True)
     pq, dq = prefill["q"], decode["q"]
     _need(pq, "prefill q", dtype=k_pool.dtype, ndim=3)
     _need(dq, "decode q", dtype=k_pool.dtype, ndim=3)

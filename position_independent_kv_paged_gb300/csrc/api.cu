@@ -91,6 +91,8 @@ minipic_status build_decode(minipic_dtype dtype, int32_t num_q_heads, const mini
   if (rotate) {
     st = check_rope(rope, kv->head_dim);
     if (st != MINIPIC_OK) return st;
+    // the tensor-core path reads the bf16 cos | sin | -sin rows
+    if (dtype == MINIPIC_BF16 && (!rope->cos_sin_bf16 || !aligned16(rope->cos_sin_bf16))) return MINIPIC_ERR_INVALID;
   }
   if (b->batch == 0) {
     *empty = true;
@@ -125,6 +127,7 @@ minipic_status build_decode(minipic_dtype dtype, int32_t num_q_heads, const mini
   a.seq_lens = b->seq_lens;
   a.q_pos = b->q_pos;
   a.cos_sin = rotate ? rope->cos_sin : nullptr;
+  a.cs_bf16 = rotate && bf16 ? rope->cos_sin_bf16 : nullptr;
   a.max_pos = rotate ? rope->max_pos : 0;
   a.out = b->out;
   a.lse = b->lse;
@@ -322,6 +325,15 @@ minipic_status minipic_rope_table_f16(uint16_t* cos_sin_f16, int32_t max_pos, in
     return MINIPIC_ERR_INVALID;
   if (!(rope_base > 0.0) || !isfinite(rope_base)) return MINIPIC_ERR_INVALID;
   cudaError_t e = launch_rope_table_f16(cos_sin_f16, max_pos, head_dim, rope_base, (cudaStream_t)stream);
+  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
+minipic_status minipic_rope_table_bf16(uint16_t* cos_sin_bf16, int32_t max_pos, int32_t head_dim,
+                                      double rope_base, minipic_stream_t stream) {
+  if (!cos_sin_bf16 || !aligned16(cos_sin_bf16) || max_pos <= 0 || head_dim <= 0 || (head_dim & 15))
+    return MINIPIC_ERR_INVALID;
+  if (!(rope_base > 0.0) || !isfinite(rope_base)) return MINIPIC_ERR_INVALID;
+  cudaError_t e = launch_rope_table_bf16(cos_sin_bf16, max_pos, head_dim, rope_base, (cudaStream_t)stream);
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 

@@ -24,10 +24,12 @@
 //
 // Rotation is factored per block: with s = slot and b = block start,
 //   (R_t q)^T (R_{b+s} k~) = (R_{t-b} q)^T (R_s k~),
-// so q is re-rotated once per block by the table row |t - b| (sin negated for
-// t < b) and each key row by the constant R_s (s < 16) held in registers.
-// This is the same algebra as rotating k~ by R_{pi(j)}; it reads one 512-byte
-// table row per block instead of sixteen.
+// so q is re-rotated once per block by the rotation of the signed angle t - b
+// and each key row by the constant R_s (s < 16) held in registers.
+// This is the same algebra as rotating k~ by R_{pi(j)}; it reads one table
+// row per block instead of sixteen.  The rows are the bf16 form of the table
+// over signed angles (cos | sin | -sin of t - b, 384 bytes at d 128): the
+// rotation reads its bf16 operands directly, whatever the sign of t - b.
 #pragma once
 
 #include <math_constants.h>
@@ -127,7 +129,7 @@ __device__ __forceinline__ uint32_t w_of(const U4& v, int k) {
 template <int D, int NW = kWarps, int NS = kStages>
 struct Smem {
   static constexpr int STAGES = NW * NS * Geo<D>::STAGE;  // K|V tiles
-  static constexpr int ROWB = 4 * D;                               // one cos|sin table row
+  static constexpr int ROWB = 3 * D;                               // one bf16 cos|sin|-sin table row
   static constexpr int ROWS = STAGES;                              // [warp][stage] table rows
   static constexpr int META = ROWS + NW * NS * ROWB;      // [split block][phys, start]
   static constexpr int kMaxSplit = 512;                            // split_blocks cap (planner)
@@ -217,9 +219,10 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   }
   const float qs = a.scale * kLog2e;  // applied to the scores; softmax runs in base 2
 
-  // R_s for the two key rows (slots g8, g8 + 8) of this thread, as packed pairs
-  // cos, sin and -sin of the slot angles of key rows g8 and g8 + 8, as bf16 pairs
-  uint32_t rcb[2][GE::NPAIR][4], rsb[2][GE::NPAIR][4], rnb[2][GE::NPAIR][4];
+  // R_s for the two key rows (slots ks0, ks0 + 8) of this thread: cos and sin
+  // of the slot angles as bf16 pairs (-sin is formed at use: holding it too
+  // would make the three-CTA build spill)
+  uint32_t rcb[2][GE::NPAIR][4], rsb[2][GE::NPAIR][4];
   int tq = 0;
   if constexpr (ROPE) {
 #pragma unroll
@@ -234,7 +237,6 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
           const float2 sn = __ldg(reinterpret_cast<const float2*>(t + D / 2 + ch.fbase[p] + 2 * e));
           rcb[row][p][e] = ptx::pack_bf16(c.x, c.y);
           rsb[row][p][e] = ptx::pack_bf16(sn.x, sn.y);
-          rnb[row][p][e] = ptx::pack_bf16(-sn.x, -sn.y);
         }
       }
     }
@@ -267,7 +269,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   cta_sync();  // meta visible, barriers initialised
 
   // lane 0: issue the k-th block of this warp into its stage: K and V tiles by
-  // TMA, plus the table row |t - start| the block's query rotation needs
+  // TMA, plus the bf16 table row of the angle t - start (row |t - start|, sign
+  // part 1 when negative) the block's query rotation needs
   auto issue = [&](int k) {
     const int i = warp + NW * k;
     const int stg = k % NS;
@@ -278,11 +281,12 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
       ptx::mbar_arrive(bar);  // nothing to load; the consumer masks the block
       return;
     }
-    int ad = 0;
+    int ad = 0, neg = 0;
     bool row_ok = false;
     if constexpr (ROPE) {
       const int delta = tq - meta[2 * i + 1];
       ad = delta < 0 ? -delta : delta;
+      neg = delta < 0 ? 1 : 0;
       row_ok = ad < a.max_pos;
     }
     ptx::mbar_arrive_expect_tx(bar, 2 * GE::TILE + (row_ok ? SM::ROWB : 0));
@@ -293,8 +297,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
       ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
     }
     if (row_ok)
-      ptx::bulk_load(sbase + SM::ROWS + (warp * NS + stg) * SM::ROWB, a.cos_sin + (size_t)ad * D, SM::ROWB,
-                     bar);
+      ptx::bulk_load(sbase + SM::ROWS + (warp * NS + stg) * SM::ROWB,
+                     a.cs_bf16 + ((size_t)ad * 2 + neg) * (3 * D / 2), SM::ROWB, bar);
   };
   if (lane == 0) {
     const int pre = nmine < NS ? nmine : NS;
@@ -341,25 +345,16 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
       break;
     }
 
-    // re-rotate q by t - start from the staged table row
+    // re-rotate q by t - start from the staged bf16 row of that signed angle
     if constexpr (ROPE) {
-      // cos and sin of |t - start| as bf16 pairs; the sign of t - start flips sin
-      const uint32_t sgn = delta < 0 ? 0x80008000u : 0u;
 #pragma unroll
       for (int p = 0; p < GE::NPAIR; ++p) {
-        const U4 c0 = ptx::lds128(rowb + 4 * ch.fbase[p]);
-        const U4 c1 = ptx::lds128(rowb + 4 * ch.fbase[p] + 16);
-        const U4 s0 = ptx::lds128(rowb + 2 * D + 4 * ch.fbase[p]);
-        const U4 s1 = ptx::lds128(rowb + 2 * D + 4 * ch.fbase[p] + 16);
-        const uint32_t cb[4] = {ptx::pack_bf16(__uint_as_float(c0.x), __uint_as_float(c0.y)),
-                                ptx::pack_bf16(__uint_as_float(c0.z), __uint_as_float(c0.w)),
-                                ptx::pack_bf16(__uint_as_float(c1.x), __uint_as_float(c1.y)),
-                                ptx::pack_bf16(__uint_as_float(c1.z), __uint_as_float(c1.w))};
-        const uint32_t sb[4] = {ptx::pack_bf16(__uint_as_float(s0.x), __uint_as_float(s0.y)) ^ sgn,
-                                ptx::pack_bf16(__uint_as_float(s0.z), __uint_as_float(s0.w)) ^ sgn,
-                                ptx::pack_bf16(__uint_as_float(s1.x), __uint_as_float(s1.y)) ^ sgn,
-                                ptx::pack_bf16(__uint_as_float(s1.z), __uint_as_float(s1.w)) ^ sgn};
-        const uint32_t nb[4] = {sb[0] ^ 0x80008000u, sb[1] ^ 0x80008000u, sb[2] ^ 0x80008000u, sb[3] ^ 0x80008000u};
+        const U4 cw = ptx::lds128(rowb + 2 * ch.fbase[p]);
+        const U4 sw = ptx::lds128(rowb + D + 2 * ch.fbase[p]);
+        const U4 nw = ptx::lds128(rowb + 2 * D + 2 * ch.fbase[p]);
+        const uint32_t cb[4] = {cw.x, cw.y, cw.z, cw.w};
+        const uint32_t sb[4] = {sw.x, sw.y, sw.z, sw.w};
+        const uint32_t nb[4] = {nw.x, nw.y, nw.z, nw.w};
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           U4 x = qraw[nt][ch.first[p]], y = qraw[nt][ch.second[p]];
@@ -381,7 +376,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
       for (int row = 0; row < 2; ++row)
 #pragma unroll
         for (int p = 0; p < GE::NPAIR; ++p)
-          rotate_pair_bf16(kr[row][ch.first[p]], kr[row][ch.second[p]], rcb[row][p], rsb[row][p], rnb[row][p]);
+        {
+          const uint32_t nn[4] = {rsb[row][p][0] ^ 0x80008000u, rsb[row][p][1] ^ 0x80008000u,
+                                  rsb[row][p][2] ^ 0x80008000u, rsb[row][p][3] ^ 0x80008000u};
+          rotate_pair_bf16(kr[row][ch.first[p]], kr[row][ch.second[p]], rcb[row][p], rsb[row][p], nn);
+        }
     }
 
     // S^T = K' Q'^T, two independent accumulation chains (even / odd k-steps)

@@ -16,6 +16,7 @@ struct DecodeArgs {
   const int32_t* seq_lens;
   const int32_t* q_pos;
   const float* cos_sin;      // [max_pos][D] or null when rotation is compiled out
+  const uint16_t* cs_bf16;   // [max_pos][2][3 D/2] bf16 cos | sin | -sin of +-p (tensor-core path), or null
   int max_pos;
   void* out;                 // [B][Hq][D]
   float* lse;                // [B][Hq] or null
@@ -56,6 +57,7 @@ enum : int { kErrBlockId = 1, kErrPosition = 2, kErrSeqLen = 4, kErrTimeout = 8,
 // Launchers; return cudaSuccess or the launch error.
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, int head_dim, double base, cudaStream_t s);
 cudaError_t launch_rope_table_f16(uint16_t* cos_sin, int max_pos, int head_dim, double base, cudaStream_t s);
+cudaError_t launch_rope_table_bf16(uint16_t* cs, int max_pos, int head_dim, double base, cudaStream_t s);
 
 // Split planning of the decode kernels (same plan used for workspace sizing).
 struct DecodePlan {

@@ -71,7 +71,7 @@ def _decode(B=1, mb=4, q=0x3000, bt=0x4000, st=0x5000, sl=0x6000, qp=0x7000, out
 
 def _call_decode(lib, dtype=1, Hq=4, kv=None, rope=None, db=None, ws=None, ws_n=0, rope_ok=True):
     kv = kv or _kv()
-    rope = rope or mp._Rope(0x9000, 1024, kv.head_dim)
+    rope = rope or mp._Rope(0x9000, 1024, kv.head_dim, None, 0xC000)
     db = db or _decode()
     return lib.minipic_attn_decode(dtype, Hq, ctypes.byref(kv), ctypes.byref(rope), ctypes.byref(db),
                                    0.0, ws, ws_n, None)
@@ -85,7 +85,7 @@ def test_decode_validation_errors(lib):
     assert _call_decode(lib, kv=_kv(bs=32)) == 2             # block size unsupported
     assert _call_decode(lib, Hq=34, kv=_kv(hkv=2)) == 2      # group of 17 > 16
     assert _call_decode(lib, kv=_kv(k=0x1001)) == 1          # misaligned pool
-    assert _call_decode(lib, rope=mp._Rope(0x9000, 1024, 64)) == 1   # table head_dim mismatch
+    assert _call_decode(lib, rope=mp._Rope(0x9000, 1024, 64, None, 0xC000)) == 1   # table head_dim mismatch
     assert _call_decode(lib, rope=mp._Rope(0, 1024, 128)) == 1       # null table
     assert _call_decode(lib, rope=mp._Rope(0x9000, 0, 128)) == 1     # empty table
     assert _call_decode(lib, db=_decode(q=0)) == 1                   # null q
@@ -94,6 +94,25 @@ def test_decode_validation_errors(lib):
     assert _call_decode(lib, db=_decode(B=-1)) == 1
     # batch 0 is a no-op
     assert _call_decode(lib, db=_decode(B=0)) == 0
+
+
+def test_bf16_decode_needs_the_bf16_table(lib):
+    # the bf16 (tensor-core) decode reads the bf16 cos | sin | -sin rows; the
+    # fp32 decode does not (its checks fail later, on the fake pointers, only
+    # for batch > 0)
+    for rope in (mp._Rope(0x9000, 1024, 128), mp._Rope(0x9000, 1024, 128, None, 0xC008)):  # missing, misaligned
+        assert _call_decode(lib, rope=rope) == 1
+        assert _call_decode(lib, rope=rope, db=_decode(B=0)) == 1
+        assert _call_decode(lib, dtype=0, rope=rope, db=_decode(B=0)) == 0
+
+
+def test_rope_table_bf16_validation(lib):
+    f = lib.minipic_rope_table_bf16
+    assert f(None, 10, 64, 1e4, None) == 1
+    assert f(0x1000, 0, 64, 1e4, None) == 1
+    assert f(0x1000, 10, 72, 1e4, None) == 1      # rows of 3 d / 2 bf16 must be whole 16-byte chunks
+    assert f(0x1000, 10, 64, 0.0, None) == 1
+    assert f(0x1008, 10, 64, 1e4, None) == 1
 
 
 def test_rope_table_validation(lib):

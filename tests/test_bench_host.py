@@ -118,3 +118,19 @@ def test_reference_arm_runs_on_rank_zero_only():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2")
     r = subprocess.run(REF_CMD, cwd=ROOT, capture_output=True, text=True, env=env, timeout=600)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_only_legs_name_known_workloads_and_calls():
+    # every --only leg (the commands the profiles are captured from) maps to a
+    # generator and a call the bench's cases provide
+    import workloads as W
+    gens = {"rag_decode", "rag_decode_private", "long_decode", "rag_prefill", "mixed_batch"}
+    for leg, (wname, kind, call) in bench.ONLY_LEGS.items():
+        assert wname in gens, leg
+        assert kind in ("decode", "prefill", "mixed"), leg
+        if kind != "mixed":
+            assert hasattr(bench.DecodeCase if kind == "decode" else bench.PrefillCase, call), leg
+    assert callable(W.rag_decode) and callable(W.mixed_batch)
+    out = subprocess.run([sys.executable, "bench.py", "--help"], cwd=ROOT, capture_output=True, text=True,
+                         check=True).stdout
+    assert "--only" in out

@@ -68,6 +68,32 @@ def test_rope_table_f16_rounds_once_to_nearest(env, d, base, max_pos):
     assert np.all(np.isfinite(Th)) and np.all(np.abs(Th) <= 1.0)
 
 
+@pytest.mark.parametrize("d,base,max_pos", [(64, 10000.0, 129), (128, 500000.0, 131073), (128, 1e6, 32769)])
+def test_rope_table_bf16_rows(env, d, base, max_pos):
+    """Rows [p, 0] and [p, 1] of the bf16 table are cos | sin | -sin of +p theta_i
+    and of -p theta_i: each value the fp32 table's value rounded to the nearest
+    bf16 (so within half a bf16 spacing plus one fp32 ulp and the fp64 angle
+    error of the oracle), with the signs placed exactly."""
+    torch, mp, dev = env
+    tab = mp.rope_table(max_pos, d, base, device=dev)
+    B = tab.cos_sin_bf16
+    assert tuple(B.shape) == (max_pos, 2, 3 * d // 2)
+    h = d // 2
+    # round to nearest even of the fp32 table (torch's conversion, not the kernel's)
+    c = tab.cos_sin[:, :h].to(torch.bfloat16)
+    s = tab.cos_sin[:, h:].to(torch.bfloat16)
+    assert torch.equal(B[:, 0, :h], c) and torch.equal(B[:, 1, :h], c)
+    assert torch.equal(B[:, 0, h:2 * h], s) and torch.equal(B[:, 0, 2 * h:], -s)
+    assert torch.equal(B[:, 1, h:2 * h], -s) and torch.equal(B[:, 1, 2 * h:], s)
+    R = oracle.rope_table(max_pos, d, base)
+    Bf = B[:, 0].float().cpu().numpy().astype(np.float64)
+    got = np.concatenate([Bf[:, :h], Bf[:, h:2 * h]], axis=1)
+    ulp32 = np.spacing(np.abs(R).astype(np.float32)).astype(np.float64)
+    half_bf16 = np.ldexp(1.0, np.frexp(np.abs(got))[1] - 9)  # half a bf16 spacing at |got|
+    angle_err = 8 * max_pos * 2.0 ** -52
+    assert np.all(np.abs(got - R) <= half_bf16 + ulp32 + angle_err)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_tiny_decode(env, dtype):
     w = W.tiny_decode(0, dtype)

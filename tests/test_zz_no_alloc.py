@@ -49,7 +49,7 @@ def _noalloc(env, w, t, rope):
     out = torch.full_like(t["q"], float("nan"))
     lse = torch.full((d.batch, w.Hq), float("nan"), dtype=torch.float32, device=dev)
     kv = mp._KV(t["k_pool"].data_ptr(), t["v_pool"].data_ptr(), *t["k_pool"].shape)
-    rp = mp._Rope(rope.cos_sin.data_ptr(), rope.max_pos, rope.head_dim)
+    rp = mp._Rope(rope.cos_sin.data_ptr(), rope.max_pos, rope.head_dim, None, rope.cos_sin_bf16.data_ptr())
     db = mp._Decode(t["q"].data_ptr(), t["block_tables"].data_ptr(), t["block_starts"].data_ptr(),
                     t["seq_lens"].data_ptr(), t["q_pos"].data_ptr(), d.batch, t["block_tables"].shape[1],
                     out.data_ptr(), lse.data_ptr())
@@ -106,6 +106,6 @@ def test_noalloc_rejects_shapes_beyond_the_fixed_scratch(env):
     assert mp.decode_workspace_size(big[0], big[1], big[2], 128, big[3]) > limit
     b, hq, hkv, mb = big
     kv = mp._KV(0x1000, 0x2000, 16, hkv, 16, 128)
-    rp = mp._Rope(0x3000, 1 << 20, 128)
+    rp = mp._Rope(0x3000, 1 << 20, 128, None, 0xA000)
     db = mp._Decode(0x4000, 0x5000, 0x6000, 0x7000, 0x8000, b, mb, 0x9000, None)
     assert fn(mp.BF16, hq, ctypes.byref(kv), ctypes.byref(rp), ctypes.byref(db), 0.0, None) == 3
