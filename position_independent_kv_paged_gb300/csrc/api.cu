@@ -234,6 +234,38 @@ minipic_status prefill_common(minipic_dtype dtype, int32_t num_q_heads, const mi
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 
+// The mixed grid runs each decode split as one CTA of 8 warps that holds a
+// whole SM (the CTA shape is the prefill's), where the standalone kernel keeps
+// 2-3 CTAs of 4 warps resident per SM.  Short splits then leave their fixed
+// cost (metadata staging, pipeline fill, merge) exposed, so the mixed grid
+// plans fewer, longer splits: about four waves of one CTA per SM, 64 to 512
+// blocks each.  Fewer splits need less of the caller's workspace, whose
+// partial-result regions are laid out again for the new split count.
+void replan_mixed_decode(DecodeArgs& a, int num_sms) {
+  if (a.n_split <= 1) return;
+  const long long total = (long long)a.batch * a.Hkv * a.max_blocks;
+  const long long slots = (long long)num_sms * 4;
+  long long est = (total + slots - 1) / slots;
+  if (est < 64) est = 64;
+  if (est > 512) est = 512;  // the decode CTA stages a split's block metadata in shared memory
+  if (est <= a.split_blocks) return;
+  int split_blocks = a.max_blocks, n_split = 1;
+  if (est < a.max_blocks) {
+    const long long n = (a.max_blocks + est - 1) / est;
+    split_blocks = (int)((a.max_blocks + n - 1) / n);
+    n_split = (a.max_blocks + split_blocks - 1) / split_blocks;
+  }
+  if (n_split >= a.n_split) return;
+  const DecodeWs ws = decode_ws_layout(a.batch, a.Hq, a.Hkv, a.D, n_split);
+  char* base = reinterpret_cast<char*>(a.counters);  // the workspace start (counters first)
+  a.split_blocks = split_blocks;
+  a.n_split = n_split;
+  if (n_split > 1) {
+    a.part_o = reinterpret_cast<float*>(base + ws.cnt_bytes);
+    a.part_ml = reinterpret_cast<float*>(base + ws.cnt_bytes + ws.o_bytes);
+  }
+}
+
 }  // namespace
 
 DecodeWs decode_ws_layout(int batch, int Hq, int Hkv, int D, int n_split) {
@@ -408,6 +440,7 @@ minipic_status minipic_attn_mixed(minipic_dtype dtype, int32_t num_q_heads, cons
     e = launch_decode(d, true, true, plan, (cudaStream_t)stream);
   } else {
     if (kv->num_blocks == 0) return MINIPIC_ERR_INVALID;
+    replan_mixed_decode(d, current_sms());
     e = launch_mixed(p, d, (cudaStream_t)stream);
   }
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
