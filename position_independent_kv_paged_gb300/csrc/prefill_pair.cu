@@ -782,13 +782,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // prefills pipelined with ongoing decodes).  Every cluster of the grid is
 // either a prefill cluster (one query-tile pair, the CTA-pair body above) or a
 // decode cluster (each of its two CTAs one decode split, the decode kernel's
-// CTA body run by warps 0-7 with 232 registers each while warps 8-15 give
-// their registers up and leave).  The decode clusters come first in the grid
+// CTA body run by warps 0-7 with 232 registers each, two stages per warp,
+// while warps 8-15 give their registers up and leave).  The decode clusters come first in the grid
 // and the prefill clusters (heaviest first) follow, so that the long prefill
 // clusters fill the SMs as the short decode CTAs drain (measured against
 // prefill first and against decode clusters spread evenly through the grid,
 // this order was the fastest).
-constexpr int kMixDecWarps = 8, kMixDecStages = 3, kMixDecBar = 8;
+constexpr int kMixDecWarps = 8, kMixDecStages = 2, kMixDecBar = 8;
 constexpr int kRegMixDec = 232, kRegMixIdle = 24;
 static_assert(2 * 128 * kRegMixDec + 2 * 128 * kRegMixIdle <= 128 * kThreads, "decode register split");
 
