@@ -326,8 +326,9 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------- GPU legs
 
-# files whose contents define the decode kernel the headline times
-DECODE_SOURCES = ("decode_mma.cu", "decode_body.cuh", "ptx.cuh")
+# files whose contents define the decode kernel the headline times and its
+# launch plan (splits, CTAs per SM)
+DECODE_SOURCES = ("decode_mma.cu", "decode_body.cuh", "ptx.cuh", "internal.h", "api.cu")
 
 
 def kernel_sources_sha256(kernel_files) -> str:
