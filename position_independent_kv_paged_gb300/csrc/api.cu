@@ -234,7 +234,7 @@ minipic_status prefill_common(minipic_dtype dtype, int32_t num_q_heads, const mi
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 
-// The mixed grid runs each decode split as one CTA of 8 warps that holds a
+// The mixed grid runs each decode split as one CTA of 8-12 warps that holds a
 // whole SM (the CTA shape is the prefill's), where the standalone kernel keeps
 // 2-3 CTAs of 4 warps resident per SM.  Short splits then leave their fixed
 // cost (metadata staging, pipeline fill, merge) exposed, so the mixed grid

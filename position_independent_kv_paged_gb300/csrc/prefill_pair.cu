@@ -782,15 +782,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // prefills pipelined with ongoing decodes).  Every cluster of the grid is
 // either a prefill cluster (one query-tile pair, the CTA-pair body above) or a
 // decode cluster (each of its two CTAs one decode split, the decode kernel's
-// CTA body run by warps 0-7 with 232 registers each, two stages per warp,
-// while warps 8-15 give their registers up and leave).  The decode clusters come first in the grid
+// CTA body with two stages per warp: for groups of up to 8 heads on warps 0-11
+// with 160 registers each while warps 12-15 give their registers up and leave,
+// for larger groups, whose body needs more registers, on warps 0-7 with 232;
+// register budgets change per warpgroup, as setmaxnreg requires).  The decode
+// clusters come first in the grid
 // and the prefill clusters (heaviest first) follow, so that the long prefill
 // clusters fill the SMs as the short decode CTAs drain (measured against
 // prefill first and against decode clusters spread evenly through the grid,
 // this order was the fastest).
-constexpr int kMixDecWarps = 8, kMixDecStages = 2, kMixDecBar = 8;
-constexpr int kRegMixDec = 232, kRegMixIdle = 24;
-static_assert(2 * 128 * kRegMixDec + 2 * 128 * kRegMixIdle <= 128 * kThreads, "decode register split");
+template <int NT>
+struct MixDec {
+  static constexpr int kWarps = NT == 1 ? 12 : 8, kStages = 2, kBar = 8;
+  static constexpr int kReg = NT == 1 ? 160 : 232, kRegIdle = NT == 1 ? 32 : 24;
+  static_assert(kWarps % 4 == 0, "setmaxnreg acts on whole warpgroups");
+  static_assert(kWarps * 32 * kReg + (16 - kWarps) * 32 * kRegIdle <= 128 * kThreads, "decode register split");
+};
 
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -800,15 +807,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long c = blockIdx.x >> 1;
   const long long d0 = c < n_dec ? c : n_dec;  // decode clusters before cluster c
   if (c < n_dec) {
-    if ((threadIdx.x >> 5) >= kMixDecWarps) {
-      regs_dec<kRegMixIdle>();
+    using MD = MixDec<NT>;
+    if ((threadIdx.x >> 5) >= MD::kWarps) {
+      regs_dec<MD::kRegIdle>();
       return;
     }
-    regs_inc<kRegMixDec>();
+    regs_inc<MD::kReg>();
     const int u = 2 * (int)d0 + (int)ptx::cluster_rank();  // decode unit: (split, kv head, request)
     if (u >= Dd.n_split * Dd.Hkv * Dd.batch) return;
     const int split = u % Dd.n_split, rest = u / Dd.n_split;
-    decode_impl::decode_cta<D, NT, true, kMixDecWarps, kMixDecStages, kMixDecBar>(&kmap, &vmap, Dd, split,
+    decode_impl::decode_cta<D, NT, true, MD::kWarps, MD::kStages, MD::kBar>(&kmap, &vmap, Dd, split,
                                                                                  rest % Dd.Hkv, rest / Dd.Hkv,
                                                                                  smem_raw);
   } else {
@@ -821,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int NT>
 cudaError_t launch_mixed_t(const PrefillArgs& p, const DecodeArgs& d, cudaStream_t s) {
-  constexpr int sa = PP<kNSK, kNSV>::TOTAL, sb = decode_impl::Smem<D, kMixDecWarps, kMixDecStages>::TOTAL;
+  constexpr int sa = PP<kNSK, kNSV>::TOTAL, sb = decode_impl::Smem<D, MixDec<NT>::kWarps, MixDec<NT>::kStages>::TOTAL;
   const int smem = (sa > sb ? sa : sb) + 1024;
   static bool done[64] = {false};
   cudaError_t e = set_smem_once(mixed_pair_kernel<NT>, smem, done);
