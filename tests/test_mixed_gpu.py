@@ -55,6 +55,21 @@ def test_mixed_scaled_matches_oracle(env):
     assert env[1].device_error() == 0
 
 
+def test_mixed_large_groups_match_oracle(env):
+    """Groups of 16 query heads per kv head: the decode CTAs of the mixed grid
+    take the layout for large groups (two n-tiles, 8 warps with 232 registers)
+    and the prefill tiles hold 8 tokens x 16 heads."""
+    w = W.mixed_batch(7, n_prefill=2, chunk=200, n_decode=5, min_ctx=1, max_ctx=3000, Hq=32, Hkv=2)
+    po, pl, do, dl, _ = run_mixed(env, w)
+    rp, rpl = oracle.prefill(w)
+    rd, rdl = oracle.decode(w)
+    compare(po, rp, "bf16", "mixed prefill part, G 16")
+    compare_lse(pl, rpl, "bf16", "mixed prefill part, G 16")
+    compare(do, rd, "bf16", "mixed decode part, G 16")
+    compare_lse(dl, rdl, "bf16", "mixed decode part, G 16")
+    assert env[1].device_error() == 0
+
+
 def test_mixed_head_dim_64_matches_oracle(env):
     """Head dim 64 runs the single-CTA prefill body with decode CTAs of the same
     shape in one grid."""
