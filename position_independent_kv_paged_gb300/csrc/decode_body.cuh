@@ -142,8 +142,10 @@ struct Smem {
 // barriers (__syncthreads) and threads beyond the working warps only do that;
 // with BAR > 0 only the first NW warps call this function and their barriers
 // are the named barrier BAR over NW * 32 threads (the other warps of the block
-// may have left).
-template <int D, int NT, bool ROPE, int NW = kWarps, int NS = kStages, int BAR = 0>
+// may have left).  With BLOCKMAP the tensor maps are 3-D views of the pools
+// (64 columns x rows x 64-column halves) and one box brings a whole K or V tile
+// of a block in the [half][key][64] layout: one copy instead of two.
+template <int D, int NT, bool ROPE, int NW = kWarps, int NS = kStages, int BAR = 0, bool BLOCKMAP = false>
 __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p,
                                            const DecodeArgs& a, const int split, const int hk, const int r,
                                            uint8_t* smem_raw) {
@@ -291,10 +293,15 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
     }
     ptx::mbar_arrive_expect_tx(bar, 2 * GE::TILE + (row_ok ? SM::ROWB : 0));
     const int y = (phys * a.Hkv + hk) * 16;
+    if constexpr (BLOCKMAP) {
+      ptx::tma_load_3d(kdst, &kmap, 0, y, 0, bar);
+      ptx::tma_load_3d(kdst + GE::TILE, &vmap, 0, y, 0, bar);
+    } else {
 #pragma unroll
-    for (int hh = 0; hh < GE::HALVES; ++hh) {
-      ptx::tma_load_2d(kdst + hh * 2048, &kmap, 64 * hh, y, bar);
-      ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
+      for (int hh = 0; hh < GE::HALVES; ++hh) {
+        ptx::tma_load_2d(kdst + hh * 2048, &kmap, 64 * hh, y, bar);
+        ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
+      }
     }
     if (row_ok)
       ptx::bulk_load(sbase + SM::ROWS + (warp * NS + stg) * SM::ROWB,

@@ -13,8 +13,8 @@ __global__ void __launch_bounds__(kWarps * 32, CPS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  decode_cta<D, NT, ROPE, kWarps, CPS == 3 ? 2 : kStages>(&kmap, &vmap, a, blockIdx.x, blockIdx.y, blockIdx.z,
-                                                          smem_raw);
+  decode_cta<D, NT, ROPE, kWarps, CPS == 3 ? 2 : kStages, 0, D == 128>(&kmap, &vmap, a, blockIdx.x, blockIdx.y,
+                                                                     blockIdx.z, smem_raw);
 }
 
 template <int D, int NT, bool ROPE, int CPS>
@@ -25,8 +25,9 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   CUtensorMap km, vm;
   const long long rows = (long long)a.num_blocks * a.Hkv * 16;
-  if (!make_pool_map(&km, a.k_pool, rows, D) || !make_pool_map(&vm, a.v_pool, rows, D))
-    return cudaErrorInvalidValue;
+  const bool ok = D == 128 ? make_pool_block_map(&km, a.k_pool, rows, D) && make_pool_block_map(&vm, a.v_pool, rows, D)
+                           : make_pool_map(&km, a.k_pool, rows, D) && make_pool_map(&vm, a.v_pool, rows, D);
+  if (!ok) return cudaErrorInvalidValue;
   dim3 grid(a.n_split, a.Hkv, a.batch);
   decode_mma_kernel<D, NT, ROPE, CPS><<<grid, kWarps * 32, smem, s>>>(km, vm, a);
   return cudaGetLastError();

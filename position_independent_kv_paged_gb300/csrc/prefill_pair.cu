@@ -802,6 +802,7 @@ struct MixDec {
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     mixed_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      const __grid_constant__ CUtensorMap kblk, const __grid_constant__ CUtensorMap vblk,
                       const PairLaunch L, const DecodeArgs Dd, const int n_pre, const int n_dec) {
   extern __shared__ uint8_t smem_raw[];
   const long long c = blockIdx.x >> 1;
@@ -816,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u = 2 * (int)d0 + (int)ptx::cluster_rank();  // decode unit: (split, kv head, request)
     if (u >= Dd.n_split * Dd.Hkv * Dd.batch) return;
     const int split = u % Dd.n_split, rest = u / Dd.n_split;
-    decode_impl::decode_cta<D, NT, true, MD::kWarps, MD::kStages, MD::kBar>(&kmap, &vmap, Dd, split,
+    decode_impl::decode_cta<D, NT, true, MD::kWarps, MD::kStages, MD::kBar, true>(&kblk, &vblk, Dd, split,
                                                                                  rest % Dd.Hkv, rest / Dd.Hkv,
                                                                                  smem_raw);
   } else {
@@ -834,9 +835,11 @@ cudaError_t launch_mixed_t(const PrefillArgs& p, const DecodeArgs& d, cudaStream
   static bool done[64] = {false};
   cudaError_t e = set_smem_once(mixed_pair_kernel<NT>, smem, done);
   if (e != cudaSuccess) return e;
-  CUtensorMap km, vm;
+  CUtensorMap km, vm, kb, vb;  // 2-D views for the prefill tiles, 3-D block views for the decode tiles
   const long long rows = (long long)p.num_blocks * p.Hkv * 16;
-  if (!make_pool_map(&km, p.k_pool, rows, D) || !make_pool_map(&vm, p.v_pool, rows, D)) return cudaErrorInvalidValue;
+  if (!make_pool_map(&km, p.k_pool, rows, D) || !make_pool_map(&vm, p.v_pool, rows, D) ||
+      !make_pool_block_map(&kb, p.k_pool, rows, D) || !make_pool_block_map(&vb, p.v_pool, rows, D))
+    return cudaErrorInvalidValue;
   PairLaunch L{p, 128 / p.G, 0};
   L.n_pairs = (p.max_q_len + 2 * L.tq - 1) / (2 * L.tq);
   const long long n_pre = (long long)L.n_pairs * p.Hkv * p.batch;
@@ -854,7 +857,7 @@ cudaError_t launch_mixed_t(const PrefillArgs& p, const DecodeArgs& d, cudaStream
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mixed_pair_kernel<NT>, km, vm, L, d, (int)n_pre, (int)n_dec);
+  return cudaLaunchKernelEx(&cfg, mixed_pair_kernel<NT>, km, vm, kb, vb, L, d, (int)n_pre, (int)n_dec);
 }
 
 template <bool ROPE>
