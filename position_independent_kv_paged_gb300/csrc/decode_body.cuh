@@ -6,21 +6,24 @@
 // pi(j) = start[r][block] + slot with a cos/sin table lookup and multiply-adds
 // per key element, then runs ordinary softmax attention.
 //
-// Layout of the work.  One CTA = (split, kv head, request); each of its 4 warps
-// owns every 4th block of the split and runs its own 3-stage TMA pipeline: the
-// (block, head) K and V tiles (16 keys x d, contiguous in the pool) arrive by
-// cp.async.bulk.tensor with 128-byte swizzle, in a [half][key][64] shared
-// layout that makes both the 16-byte key-row reads and the transposing
-// ldmatrix reads of V free of bank conflicts.
+// Layout of the work.  One CTA = (split, kv head, request); each of its warps
+// owns every NW-th block of the split and runs its own TMA ring of NS stages
+// (the standalone kernel: 4 warps, 2 stages with 3 CTAs per SM or 3 stages with
+// 2): the (block, head) K and V tiles (16 keys x d, contiguous in the pool)
+// arrive by cp.async.bulk.tensor with 128-byte swizzle (at head dim 128 one box
+// per tile over a 3-D view of the pool), in a [half][key][64] shared layout
+// that makes both the 16-byte key-row reads and the transposing ldmatrix reads
+// of V free of bank conflicts.
 //
 // Per 16-key block and GQA group (up to 8 query heads per n-tile):
 //   S^T[key][head] = K'[key][:] . Q'[head][:]  (mma m16n8k16, M = the 16 keys)
 //   O^T[dim][head] += V^T[dim][key] P^T[key][head]
 // K' is formed in registers: rows are read from shared memory and rotated in
 // packed bf16 arithmetic (two bf16x2 multiply / multiply-adds per pair of
-// elements) straight into the MMA's bf16 A operand; Q' likewise.  The contraction order of the head dimension is a per-thread
-// permutation chosen so that each rotary pair (i, i + d/2) is thread-local;
-// Q' uses the same permutation.
+// elements) straight into the MMA's bf16 A operand; Q' likewise.  The
+// contraction order of the head dimension is a per-thread permutation chosen
+// so that each rotary pair (i, i + d/2) is thread-local; Q' uses the same
+// permutation.
 //
 // Rotation is factored per block: with s = slot and b = block start,
 //   (R_t q)^T (R_{b+s} k~) = (R_{t-b} q)^T (R_s k~),
