@@ -180,3 +180,40 @@ def test_kv_swap_validation(lib):
         assert f(1, ctypes.byref(KV(None, None, 4, 2, 16, 80)), None, 1, None, None, None) == 2
         assert f(1, ctypes.byref(kv), None, -1, None, None, None) == 1     # negative count
         assert f(1, ctypes.byref(kv), None, 3, None, None, None) == 1      # missing pointers
+
+
+def test_plain_c_program_uses_the_host_calls(lib, tmp_path):
+    """include/minipic.h compiles as strict C99 and a C program linked against
+    libminipic.so gets the block hashes and prefix-cache tables the oracle gives
+    (SSEP span shared at two offsets)."""
+    import shutil
+    import subprocess
+
+    import numpy as np
+
+    import oracle.blockhash as bh
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(mp.library_path())
+    exe = str(tmp_path / "abi_from_c")
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "csrc", "abi_from_c.c"), "-L", libdir, "-l:libminipic.so",
+                    "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.splitlines()
+    rec = {ln.split()[0]: ln.split()[1:] for ln in out}
+    assert rec["status"] == ["invalid", "argument"] and rec["workspace"] == ["1"] and "done" in rec
+    ssep, pdep, bs = -7, -9, 4
+    p1 = [1, 2, 3, 4, ssep, 11, 12, 13, pdep, 21, 22, 23, 5, 6]
+    p2 = [7, 7, 7, 7, 8, 8, 8, 8, ssep, 11, 12, 13, pdep, 31, 32, 33]
+    h1 = bh.block_hashes(p1, bs, ssep, pdep, 0x1234)
+    h2 = bh.block_hashes(p2, bs, ssep, pdep, 0x1234)
+    assert [int(x) for x in rec["hashes1"]] == h1 and [int(x) for x in rec["hashes2"]] == h2
+    cache = bh.PrefixCache(16)
+    for key, hs in (("tables1", h1), ("tables2", h2)):
+        t, s, f = cache.assign(hs, 4, bs)
+        want = [f"{int(a)}:{int(b)}:{int(c)}" for a, b, c in zip(t, s, f)]
+        assert rec[key] == want, key
+    assert h1[1] == h2[2] and rec["tables1"][1].split(":")[0] == rec["tables2"][2].split(":")[0]
+    assert np.int64(rec["tables1"][1].split(":")[1]) != np.int64(rec["tables2"][2].split(":")[1])
