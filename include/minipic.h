@@ -195,6 +195,14 @@ minipic_status minipic_rope_table_f16(uint16_t* cos_sin_f16, int32_t max_pos, in
 minipic_status minipic_rope_table_bf16(uint16_t* cos_sin_bf16, int32_t max_pos, int32_t head_dim,
                                        double rope_base, minipic_stream_t stream);
 
+/* The three forms of the table in one pass (one fp64 sincos per entry):
+ * any of cos_sin (as minipic_rope_table), cos_sin_f16 (as _f16) and
+ * cos_sin_bf16 (as _bf16) may be NULL, not all three; the values are those of
+ * the single-form calls.  Errors as for those calls. */
+minipic_status minipic_rope_tables(float* cos_sin, uint16_t* cos_sin_f16, uint16_t* cos_sin_bf16,
+                                   int32_t max_pos, int32_t head_dim, double rope_base,
+                                   minipic_stream_t stream);
+
 /* Workspace bytes minipic_attn_decode needs for this shape on the current
  * device (split-KV partial results).  0 means no workspace is needed.  The
  * value depends only on the arguments and the device's SM count. */

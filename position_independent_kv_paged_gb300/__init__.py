@@ -122,6 +122,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         L.minipic_rope_table_f16.argtypes = [c_vp, c_i32, c_i32, c_d, c_vp]
         L.minipic_rope_table_bf16.restype = ctypes.c_int
         L.minipic_rope_table_bf16.argtypes = [c_vp, c_i32, c_i32, c_d, c_vp]
+        L.minipic_rope_tables.restype = ctypes.c_int
+        L.minipic_rope_tables.argtypes = [c_vp, c_vp, c_vp, c_i32, c_i32, c_d, c_vp]
         L.minipic_attn_decode_workspace_size.restype = c_sz
         L.minipic_attn_decode_workspace_size.argtypes = [c_i32] * 6
         L.minipic_attn_decode.restype = ctypes.c_int
@@ -271,14 +273,17 @@ def rope_table_bf16(max_pos: int, head_dim: int, base: float, device=None, strea
 
 
 def rope_table(max_pos: int, head_dim: int, base: float, device=None, stream=None) -> RopeTable:
-    """Build the cos/sin table (float32, float16 and bfloat16 forms) on the GPU."""
+    """Build the cos/sin table (float32, float16 and bfloat16 forms) on the GPU
+    in one pass."""
     torch = _torch()
     L = load()
-    f32 = torch.empty((max_pos, head_dim), dtype=torch.float32, device=device if device is not None else "cuda")
-    _check(L.minipic_rope_table(f32.data_ptr(), int(max_pos), int(head_dim), float(base), _stream(stream)),
-           "minipic_rope_table")
-    return RopeTable(f32, rope_table_f16(max_pos, head_dim, base, device=f32.device, stream=stream),
-                     rope_table_bf16(max_pos, head_dim, base, device=f32.device, stream=stream))
+    dev = device if device is not None else "cuda"
+    f32 = torch.empty((max_pos, head_dim), dtype=torch.float32, device=dev)
+    f16 = torch.empty((max_pos, head_dim), dtype=torch.float16, device=f32.device)
+    b16 = torch.empty((max_pos, 2, 3 * head_dim // 2), dtype=torch.bfloat16, device=f32.device)
+    _check(L.minipic_rope_tables(f32.data_ptr(), f16.data_ptr(), b16.data_ptr(), int(max_pos), int(head_dim),
+                                 float(base), _stream(stream)), "minipic_rope_tables")
+    return RopeTable(f32, f16, b16)
 
 
 def _rope_struct(rope, need_f16: bool, need_bf16: bool = False) -> _Rope:

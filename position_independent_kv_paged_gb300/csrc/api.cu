@@ -360,6 +360,19 @@ minipic_status minipic_rope_table_f16(uint16_t* cos_sin_f16, int32_t max_pos, in
   return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
 }
 
+minipic_status minipic_rope_tables(float* cos_sin, uint16_t* cos_sin_f16, uint16_t* cos_sin_bf16, int32_t max_pos,
+                                   int32_t head_dim, double rope_base, minipic_stream_t stream) {
+  if (!cos_sin && !cos_sin_f16 && !cos_sin_bf16) return MINIPIC_ERR_INVALID;
+  if ((cos_sin && !aligned16(cos_sin)) || (cos_sin_f16 && !aligned16(cos_sin_f16)) ||
+      (cos_sin_bf16 && !aligned16(cos_sin_bf16)))
+    return MINIPIC_ERR_INVALID;
+  if (max_pos <= 0 || head_dim <= 0 || (head_dim & 1) || (cos_sin_bf16 && (head_dim & 15))) return MINIPIC_ERR_INVALID;
+  if (!(rope_base > 0.0) || !isfinite(rope_base)) return MINIPIC_ERR_INVALID;
+  cudaError_t e = launch_rope_tables(cos_sin, cos_sin_f16, cos_sin_bf16, max_pos, head_dim, rope_base,
+                                     (cudaStream_t)stream);
+  return e == cudaSuccess ? MINIPIC_OK : MINIPIC_ERR_CUDA;
+}
+
 minipic_status minipic_rope_table_bf16(uint16_t* cos_sin_bf16, int32_t max_pos, int32_t head_dim,
                                       double rope_base, minipic_stream_t stream) {
   if (!cos_sin_bf16 || !aligned16(cos_sin_bf16) || max_pos <= 0 || head_dim <= 0 || (head_dim & 15))

@@ -58,6 +58,8 @@ enum : int { kErrBlockId = 1, kErrPosition = 2, kErrSeqLen = 4, kErrTimeout = 8,
 cudaError_t launch_rope_table(float* cos_sin, int max_pos, int head_dim, double base, cudaStream_t s);
 cudaError_t launch_rope_table_f16(uint16_t* cos_sin, int max_pos, int head_dim, double base, cudaStream_t s);
 cudaError_t launch_rope_table_bf16(uint16_t* cs, int max_pos, int head_dim, double base, cudaStream_t s);
+cudaError_t launch_rope_tables(float* f32, uint16_t* f16, uint16_t* b16, int max_pos, int head_dim, double base,
+                               cudaStream_t s);
 
 // Split planning of the decode kernels (same plan used for workspace sizing).
 struct DecodePlan {

@@ -42,7 +42,8 @@ def test_binding_covers_the_entry_points():
     c_only = {"minipic_attn_decode_noalloc", "minipic_status_string", "minipic_prefix_cache_create",
               "minipic_prefix_cache_destroy", "minipic_prefix_cache_assign", "minipic_prefix_cache_release"}
     renamed = {"minipic_attn_decode_workspace_size": "decode_workspace_size",
-               "minipic_attn_prefill_workspace_size": "prefill_workspace_size"}
+               "minipic_attn_prefill_workspace_size": "prefill_workspace_size",
+               "minipic_rope_tables": "rope_table"}
     for n in declared_functions():
         if n in c_only:
             continue
@@ -113,6 +114,16 @@ def test_rope_table_bf16_validation(lib):
     assert f(0x1000, 10, 72, 1e4, None) == 1      # rows of 3 d / 2 bf16 must be whole 16-byte chunks
     assert f(0x1000, 10, 64, 0.0, None) == 1
     assert f(0x1008, 10, 64, 1e4, None) == 1
+
+
+def test_rope_tables_validation(lib):
+    f = lib.minipic_rope_tables
+    assert f(None, None, None, 10, 64, 1e4, None) == 1          # no table asked for
+    assert f(0x1004, None, None, 10, 64, 1e4, None) == 1        # misaligned
+    assert f(None, 0x1008, None, 10, 64, 1e4, None) == 1
+    assert f(None, None, 0x1000, 10, 72, 1e4, None) == 1        # bf16 rows need head_dim % 16 == 0
+    assert f(0x1000, 0x2000, 0x3000, 0, 64, 1e4, None) == 1
+    assert f(0x1000, 0x2000, 0x3000, 10, 64, -1.0, None) == 1
 
 
 def test_rope_table_validation(lib):

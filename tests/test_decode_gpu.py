@@ -94,6 +94,20 @@ def test_rope_table_bf16_rows(env, d, base, max_pos):
     assert np.all(np.abs(got - R) <= half_bf16 + ulp32 + angle_err)
 
 
+def test_rope_tables_one_pass_equals_the_single_forms(env):
+    """minipic_rope_tables writes the same bits as the three single-form calls."""
+    torch, mp, dev = env
+    tab = mp.rope_table(4097, 128, 500000.0, device=dev)
+    f32 = torch.empty_like(tab.cos_sin)
+    assert mp.load().minipic_rope_table(f32.data_ptr(), 4097, 128, 500000.0, None) == 0
+    f16 = mp.rope_table_f16(4097, 128, 500000.0, device=dev)
+    b16 = mp.rope_table_bf16(4097, 128, 500000.0, device=dev)
+    torch.cuda.synchronize()
+    assert torch.equal(f32.view(torch.int32), tab.cos_sin.view(torch.int32))
+    assert torch.equal(f16.view(torch.int16), tab.cos_sin_f16.view(torch.int16))
+    assert torch.equal(b16.view(torch.int16), tab.cos_sin_bf16.view(torch.int16))
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_tiny_decode(env, dtype):
     w = W.tiny_decode(0, dtype)
