@@ -109,7 +109,7 @@ struct PP {
   static_assert(TOTAL + 1024 <= 232448, "shared memory");
 };
 
-constexpr int kNSK = 4, kNSV = 3;
+constexpr int kNSK = 4, kNSV = 2;
 
 struct PairLaunch {
   PrefillArgs a;
