@@ -299,12 +299,18 @@ DecodePlan plan_decode(int batch, int Hkv, int G, int D, int max_blocks, int bs,
   // tensor-core path: CTAs of 4 warps; with many (request, kv head) pairs, 3
   // resident per SM with 2 stages per warp (more warps to hide the per-block
   // latency when blocks come from L2), else 2 per SM with 3 stages (deeper
-  // per-warp prefetch for HBM-bound long contexts); 1 for groups > 8.  ~12
-  // waves of CTAs, each split at least 32 blocks (8 per warp)
+  // per-warp prefetch for HBM-bound long contexts); 1 for groups > 8.  Splits
+  // of at least 32 blocks (8 per warp), as long as about 4 waves of CTAs (3
+  // with 2 CTAs per SM) allow: each split pays a fixed cost (metadata
+  // staging, pipeline fill, the merge), so longer splits won over the ~12 waves
+  // used before (Zipf-shared RAG batch 0.259 -> 0.221 ms, long contexts 0.631
+  // -> 0.565 ms); groups > 8 keep ~12 waves.  The table width stands in for
+  // the lengths, which stay on the device.
   p.ctas_per_sm = G > 8 ? 1 : (pairs >= 2LL * num_sms ? 3 : 2);
   const long long resident = (long long)num_sms * p.ctas_per_sm;
   const long long total = pairs * max_blocks;
-  long long est = (total + resident * 12 - 1) / (resident * 12);
+  const long long waves = p.ctas_per_sm == 3 ? 4 : (p.ctas_per_sm == 2 ? 3 : 12);
+  long long est = (total + resident * waves - 1) / (resident * waves);
   if (est < 32) est = 32;
   if (est > 512) est = 512;  // the kernel stages a split's block metadata in shared memory
   if (est >= max_blocks) return p;
