@@ -186,20 +186,76 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
   const int span = b_end - b_begin;
   const int nmine = (worker && span > warp) ? (span - warp + NW - 1) / NW : 0;
 
-  // block ids and start positions of the whole split, staged once
+  // lane 0: issue the k-th block of this warp (physical block phys, start
+  // position start, query position tqv) into its stage: K and V tiles by TMA,
+  // plus the bf16 table row of the angle tqv - start (row |tqv - start|, sign
+  // part 1 when negative) the block's query rotation needs
+  auto issue_blk = [&](int k, int phys, int start, int tqv) {
+    const int stg = k % NS;
+    const uint32_t bar = bar_base + (warp * NS + stg) * 8;
+    const uint32_t kdst = sbase + (warp * NS + stg) * GE::STAGE;
+    if (phys < 0 || phys >= a.num_blocks) {
+      ptx::mbar_arrive(bar);  // nothing to load; the consumer masks the block
+      return;
+    }
+    int ad = 0, neg = 0;
+    bool row_ok = false;
+    if constexpr (ROPE) {
+      const int delta = tqv - start;
+      ad = delta < 0 ? -delta : delta;
+      neg = delta < 0 ? 1 : 0;
+      row_ok = ad < a.max_pos;
+    }
+    ptx::mbar_arrive_expect_tx(bar, 2 * GE::TILE + (row_ok ? SM::ROWB : 0));
+    const int y = (phys * a.Hkv + hk) * 16;
+    if constexpr (BLOCKMAP) {
+      ptx::tma_load_3d(kdst, &kmap, 0, y, 0, bar);
+      ptx::tma_load_3d(kdst + GE::TILE, &vmap, 0, y, 0, bar);
+    } else {
+#pragma unroll
+      for (int hh = 0; hh < GE::HALVES; ++hh) {
+        ptx::tma_load_2d(kdst + hh * 2048, &kmap, 64 * hh, y, bar);
+        ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
+      }
+    }
+    if (row_ok)
+      ptx::bulk_load(sbase + SM::ROWS + (warp * NS + stg) * SM::ROWB,
+                     a.cs_bf16 + ((size_t)ad * 2 + neg) * (3 * D / 2), SM::ROWB, bar);
+  };
+
+  // Each worker warp's lane 0 initialises its stage barriers.  With 3 stages
+  // or more (the standalone layout for HBM-bound long contexts) it also starts
+  // the copies of its first blocks at once, from the table entries in global
+  // memory, so that they overlap the staging and the query setup below (the
+  // staged entries serve the later blocks).  Measured: long contexts 0.563 ->
+  // 0.544 ms; with 2 stages (L2-served batches, the mixed grid) it was slower.
+  constexpr bool kEarly = NS >= 3 && BAR == 0;
   {
     const int* bt = a.block_tables + (size_t)r * mb + b_begin;
     const int* bs_ = a.block_starts + (size_t)r * mb + b_begin;
+    if (worker && lane == 0) {
+#pragma unroll
+      for (int st = 0; st < NS; ++st) ptx::mbar_init(bar_base + (warp * NS + st) * 8, 1);
+      ptx::fence_barrier_init();
+      ptx::fence_proxy_async_smem();
+    }
+    if (kEarly && worker && lane == 0) {
+      int tq0 = 0;
+      if constexpr (ROPE) {
+        tq0 = a.q_pos[r];
+        if (tq0 < 0 || tq0 >= a.max_pos) tq0 = 0;  // flagged below; the same value the loop uses
+      }
+      const int pre = nmine < NS ? nmine : NS;
+      for (int k = 0; k < pre; ++k) {
+        const int i = warp + NW * k;
+        issue_blk(k, __ldg(bt + i), ROPE ? __ldg(bs_ + i) : 0, tq0);
+      }
+    }
+    // block ids and start positions of the whole split, staged once
     for (int i = threadIdx.x; i < span; i += nthr) {
       meta[2 * i] = __ldg(bt + i);
       meta[2 * i + 1] = ROPE ? __ldg(bs_ + i) : 0;
     }
-  }
-  if (worker && lane == 0) {
-#pragma unroll
-    for (int st = 0; st < NS; ++st) ptx::mbar_init(bar_base + (warp * NS + st) * 8, 1);
-    ptx::fence_barrier_init();
-    ptx::fence_proxy_async_smem();
   }
 
   const Chunks<D> ch(tig);
@@ -271,46 +327,14 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap* kmap_p, const CUte
       for (int k = 0; k < 4; ++k) oacc[mt][nt][k] = 0.f;
   }
 
-  cta_sync();  // meta visible, barriers initialised
+  cta_sync();  // meta visible
 
-  // lane 0: issue the k-th block of this warp into its stage: K and V tiles by
-  // TMA, plus the bf16 table row of the angle t - start (row |t - start|, sign
-  // part 1 when negative) the block's query rotation needs
+  // lane 0: issue the k-th block of this warp (from the staged entries)
   auto issue = [&](int k) {
     const int i = warp + NW * k;
-    const int stg = k % NS;
-    const uint32_t bar = bar_base + (warp * NS + stg) * 8;
-    const uint32_t kdst = sbase + (warp * NS + stg) * GE::STAGE;
-    const int phys = meta[2 * i];
-    if (phys < 0 || phys >= a.num_blocks) {
-      ptx::mbar_arrive(bar);  // nothing to load; the consumer masks the block
-      return;
-    }
-    int ad = 0, neg = 0;
-    bool row_ok = false;
-    if constexpr (ROPE) {
-      const int delta = tq - meta[2 * i + 1];
-      ad = delta < 0 ? -delta : delta;
-      neg = delta < 0 ? 1 : 0;
-      row_ok = ad < a.max_pos;
-    }
-    ptx::mbar_arrive_expect_tx(bar, 2 * GE::TILE + (row_ok ? SM::ROWB : 0));
-    const int y = (phys * a.Hkv + hk) * 16;
-    if constexpr (BLOCKMAP) {
-      ptx::tma_load_3d(kdst, &kmap, 0, y, 0, bar);
-      ptx::tma_load_3d(kdst + GE::TILE, &vmap, 0, y, 0, bar);
-    } else {
-#pragma unroll
-      for (int hh = 0; hh < GE::HALVES; ++hh) {
-        ptx::tma_load_2d(kdst + hh * 2048, &kmap, 64 * hh, y, bar);
-        ptx::tma_load_2d(kdst + GE::TILE + hh * 2048, &vmap, 64 * hh, y, bar);
-      }
-    }
-    if (row_ok)
-      ptx::bulk_load(sbase + SM::ROWS + (warp * NS + stg) * SM::ROWB,
-                     a.cs_bf16 + ((size_t)ad * 2 + neg) * (3 * D / 2), SM::ROWB, bar);
+    issue_blk(k, meta[2 * i], meta[2 * i + 1], tq);
   };
-  if (lane == 0) {
+  if (!kEarly && lane == 0) {
     const int pre = nmine < NS ? nmine : NS;
     for (int k = 0; k < pre; ++k) issue(k);
   }
