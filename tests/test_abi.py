@@ -228,3 +228,26 @@ def test_plain_c_program_uses_the_host_calls(lib, tmp_path):
         assert rec[key] == want, key
     assert h1[1] == h2[2] and rec["tables1"][1].split(":")[0] == rec["tables2"][2].split(":")[0]
     assert np.int64(rec["tables1"][1].split(":")[1]) != np.int64(rec["tables2"][2].split(":")[1])
+
+
+def test_binding_has_no_cpu_fallback(lib):
+    """Every attention entry of the binding refuses host tensors (no CPU path
+    exists), and a missing library is an error, not a silent fallback."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(2, 4, 128, dtype=torch.bfloat16)
+    pool = torch.zeros(4, 2, 16, 128, dtype=torch.bfloat16)
+    i32 = torch.zeros(2, 4, dtype=torch.int32)
+    v32 = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mp.attn_decode(q, pool, pool, i32, i32, v32, v32, torch.zeros(16, 128))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mp.attn_prefill(q, torch.zeros(3, dtype=torch.int32), v32, pool, pool, i32, i32, v32,
+                        torch.zeros(16, 128), max_q_len=1)
+    import importlib
+    import subprocess
+    import sys
+    code = ("import position_independent_kv_paged_gb300 as mp\n"
+            "try:\n    mp.load('/nonexistent/libminipic.so')\nexcept mp.MiniPICError as e:\n    print('refused')\n")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True).stdout
+    assert "refused" in out
+    importlib.import_module("position_independent_kv_paged_gb300")
